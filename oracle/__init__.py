@@ -1,0 +1,255 @@
+"""Python view of the CPU oracle (``nvfp4_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
+baseline leg may use this module; the library under ``nvfp4_w4a16_moe_gb300``
+never does. It shares no code with the CUDA path; the only thing both sides
+import is the seeded input generator in ``workload``.
+
+Every function converts arrays to contiguous numpy buffers, calls the C code
+and returns numpy arrays. All results are fp64 unless they are codes/bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "nvfp4_oracle.c")
+LIB = os.path.join(HERE, "_liboracle.so")
+
+SCALE_E4M3 = 0
+SCALE_FP16 = 1
+
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+          "-Wall", "-Wextra", "-Wno-unused-parameter"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no CUDA involved)."""
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(LIB)
+        P = ctypes.c_void_p
+        i32, f32 = ctypes.c_int, ctypes.c_float
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [i32]
+        L.orc_e2m1_encode.restype = i32
+        L.orc_e2m1_encode.argtypes = [f32]
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_e4m3_decode.argtypes = [i32]
+        L.orc_e4m3_encode.restype = i32
+        L.orc_e4m3_encode.argtypes = [f32]
+        L.orc_fp16_decode.restype = ctypes.c_double
+        L.orc_fp16_decode.argtypes = [i32]
+        L.orc_fp16_encode.restype = i32
+        L.orc_fp16_encode.argtypes = [f32]
+        L.orc_pack.restype = i32
+        L.orc_pack.argtypes = [P, i32, i32, i32, P, P, P]
+        L.orc_dequant.restype = None
+        L.orc_dequant.argtypes = [P, P, f32, i32, i32, i32, P]
+        L.orc_gemv.restype = None
+        L.orc_gemv.argtypes = [P, P, f32, i32, i32, i32, P, i32, P]
+        L.orc_router_logits.restype = None
+        L.orc_router_logits.argtypes = [P, i32, i32, P, i32, P]
+        L.orc_route.restype = i32
+        L.orc_route.argtypes = [P, i32, i32, i32, P, P, P]
+        L.orc_swiglu.restype = None
+        L.orc_swiglu.argtypes = [P, P, f32, P, P, f32, P, P, f32, i32, i32, i32, P, i32, P]
+        L.orc_moe_layer.restype = i32
+        L.orc_moe_layer.argtypes = ([i32] * 6 + [P, i32, P, P] + [P, P, P] * 3 +
+                                    [P, P, f32] * 3 + [P, P, P, P, P])
+        _lib = L
+    return _lib
+
+
+def _np(a, dtype):
+    """Contiguous numpy copy/view of a numpy array or CPU torch tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu()
+        if str(a.dtype) == "torch.bfloat16":
+            a = a.view(__import__("torch").int16).numpy().view(np.uint16)
+        else:
+            a = a.numpy()
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------- formats
+
+def e2m1_decode(code: int) -> float:
+    return lib().orc_e2m1_decode(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().orc_e2m1_encode(float(v))
+
+
+def e4m3_decode(b: int) -> float:
+    return lib().orc_e4m3_decode(int(b))
+
+
+def e4m3_encode(v: float) -> int:
+    return lib().orc_e4m3_encode(float(v))
+
+
+def fp16_decode(b: int) -> float:
+    return lib().orc_fp16_decode(int(b))
+
+
+def fp16_encode(v: float) -> int:
+    return lib().orc_fp16_encode(float(v))
+
+
+@dataclass
+class Packed:
+    """One NVFP4 matrix: packed [N, K/2] u8, scales [N, K/16] (u8 E4M3 or u16 FP16), fp32 tensor scale."""
+    packed: np.ndarray
+    scales: np.ndarray
+    tensor_scale: float
+    kind: int
+    N: int
+    K: int
+
+
+def pack(w, kind: int = SCALE_E4M3) -> Packed:
+    w = _np(w, np.float32)
+    N, K = w.shape
+    packed = np.zeros((N, K // 2), np.uint8)
+    scales = np.zeros((N, K // 16), np.uint8 if kind == SCALE_E4M3 else np.uint16)
+    ts = np.zeros(1, np.float32)
+    rc = lib().orc_pack(_ptr(w), N, K, kind, _ptr(packed), _ptr(scales), _ptr(ts))
+    if rc != 0:
+        raise ValueError("oracle pack failed: code %d" % rc)
+    return Packed(packed, scales, float(ts[0]), kind, N, K)
+
+
+def dequant(p: Packed) -> np.ndarray:
+    out = np.zeros((p.N, p.K), np.float64)
+    lib().orc_dequant(_ptr(p.packed), _ptr(p.scales), p.tensor_scale, p.kind, p.N, p.K, _ptr(out))
+    return out
+
+
+def gemv(p: Packed, x) -> np.ndarray:
+    """y[T, N] (fp64) = dequant(p) @ x[T, K] (bf16)."""
+    xb = _np(x, np.uint16)
+    T = xb.shape[0]
+    y = np.zeros((T, p.N), np.float64)
+    lib().orc_gemv(_ptr(p.packed), _ptr(p.scales), p.tensor_scale, p.kind, p.N, p.K, _ptr(xb), T,
+                   _ptr(y))
+    return y
+
+
+def router_logits(x, router_w) -> np.ndarray:
+    xb = _np(x, np.uint16)
+    wb = _np(router_w, np.uint16)
+    T, H = xb.shape
+    E = wb.shape[0]
+    out = np.zeros((T, E), np.float64)
+    lib().orc_router_logits(_ptr(xb), T, H, _ptr(wb), E, _ptr(out))
+    return out
+
+
+def route(logits, k: int):
+    """(ids [T,k] int32, w [T,k] fp64, p [T,E] fp64) from fp64 logits [T,E]."""
+    lg = _np(logits, np.float64)
+    T, E = lg.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    p = np.zeros((T, E), np.float64)
+    rc = lib().orc_route(_ptr(lg), T, E, k, _ptr(ids), _ptr(w), _ptr(p))
+    if rc != 0:
+        raise ValueError("oracle route failed: code %d" % rc)
+    return ids, w, p
+
+
+def swiglu(g: Packed, u: Packed, d: Packed, x) -> np.ndarray:
+    xb = _np(x, np.uint16)
+    T, H = xb.shape
+    I = g.N
+    y = np.zeros((T, H), np.float64)
+    lib().orc_swiglu(_ptr(g.packed), _ptr(g.scales), g.tensor_scale, _ptr(u.packed), _ptr(u.scales),
+                     u.tensor_scale, _ptr(d.packed), _ptr(d.scales), d.tensor_scale, g.kind, H, I,
+                     _ptr(xb), T, _ptr(y))
+    return y
+
+
+@dataclass
+class LayerResult:
+    y: np.ndarray        # [T, H] fp64
+    ids: np.ndarray      # [T, k] int32
+    w: np.ndarray        # [T, k] fp64
+    sigmoid: np.ndarray  # [T] fp64
+
+
+def moe_layer(x, router_w, sh_gate_vec, experts: dict, shared, k: int, kind: int = SCALE_E4M3,
+              force_ids=None) -> LayerResult:
+    """The full layer. ``experts`` maps expert id -> (gate, up, down) ``Packed``;
+    only the experts that routing selects need to be present. ``shared`` is
+    (gate, up, down) ``Packed`` or None for a layer without shared expert."""
+    xb = _np(x, np.uint16)
+    wg = _np(router_w, np.uint16)
+    T, H = xb.shape
+    E = wg.shape[0]
+    any_e = next(iter(experts.values())) if experts else None
+    I = any_e[0].N if any_e is not None else 1
+    arrs = {n: (ctypes.c_void_p * E)() for n in ("gp", "gs", "up", "us", "dp", "ds")}
+    ts = {n: np.zeros(E, np.float32) for n in ("g", "u", "d")}
+    keep = []
+    for e, (g, u, d) in experts.items():
+        for name, p in (("g", g), ("u", u), ("d", d)):
+            arrs[name + "p"][e] = p.packed.ctypes.data
+            arrs[name + "s"][e] = p.scales.ctypes.data
+            ts[name][e] = p.tensor_scale
+            keep.append(p)
+    if shared is not None:
+        sg, su, sd = shared
+        Is = sg.N
+        sh = [(_ptr(m.packed), _ptr(m.scales), m.tensor_scale) for m in (sg, su, sd)]
+        sgv = _np(sh_gate_vec, np.uint16)
+    else:
+        Is = 0
+        sh = [(None, None, 0.0)] * 3
+        sgv = np.zeros(H, np.uint16)
+    y = np.zeros((T, H), np.float64)
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    sig = np.zeros(T, np.float64)
+    fi = None if force_ids is None else _np(force_ids, np.int32)
+    rc = lib().orc_moe_layer(
+        H, E, k, I, Is, kind, _ptr(xb), T, _ptr(wg), _ptr(sgv),
+        arrs["gp"], arrs["gs"], _ptr(ts["g"]), arrs["up"], arrs["us"], _ptr(ts["u"]),
+        arrs["dp"], arrs["ds"], _ptr(ts["d"]),
+        sh[0][0], sh[0][1], sh[0][2], sh[1][0], sh[1][1], sh[1][2], sh[2][0], sh[2][1], sh[2][2],
+        None if fi is None else _ptr(fi), _ptr(y), _ptr(ids), _ptr(w), _ptr(sig))
+    if rc == 3:
+        raise KeyError("routing selected an expert that was not provided")
+    if rc != 0:
+        raise ValueError("oracle moe_layer failed: code %d" % rc)
+    return LayerResult(y, ids, w, sig)
+
+
+def logit_gap(logits, k: int) -> np.ndarray:
+    """Per token, the gap between the k-th and (k+1)-th largest logit (inf if E == k)."""
+    lg = np.sort(_np(logits, np.float64), axis=1)[:, ::-1]
+    if lg.shape[1] <= k:
+        return np.full(lg.shape[0], np.inf)
+    return lg[:, k - 1] - lg[:, k]
