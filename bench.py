@@ -1,0 +1,321 @@
+"""Benchmark: single-token decode through a Qwen3.6-35B-A3B-shaped NVFP4 MoE layer.
+
+One step = one token through one MoE layer (router GEMV, softmax-all -> top-8 ->
+renormalise, 8 routed SwiGLU experts + sigmoid-gated shared expert, combine),
+hidden 2048, 256 experts, intermediate 512, E4M3 block scales. Steps rotate over
+32 independently seeded layer instances (seeds 0..31, ~14.5 GB of packed
+weights), so consecutive steps never hit the same weights in L2 (129 MB).
+
+Prints one JSON line. ``--impl reference`` times the CPU oracle instead (the
+reference arm for this build), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 MoE-layer decode: µs/token and achieved HBM GB/s as % of GB300 peak"
+UNIT = "us/token"
+N_SEEDS = 32
+WORKLOAD = ("qwen3.6-35b-a3b-shaped MoE layer decode, T=1 token/step, H=2048 E=256 top-8 I=512 "
+            "shared Is=512 sigmoid gate, NVFP4 E4M3 per-16 scales, seeds 0..31")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (median SM clock, throttle reasons)."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------ oracle arm
+
+def cpu_oracle_sample(budget_s: float, max_tokens: int = 64):
+    """Time the CPU oracle on single tokens of the same workload (weights packed
+    beforehand, as the GPU's are). Returns (us_per_token, tokens, cores)."""
+    import oracle
+    import workload as wl
+    import numpy as np
+    shape = wl.QWEN36_35B_A3B
+    times = []
+    t_start = time.time()
+    seed = 0
+    while len(times) < max_tokens and (time.time() - t_start) < budget_s:
+        L = wl.LayerInputs(shape, seed=seed % N_SEEDS)
+        x = wl.activations(seed % N_SEEDS, 1, shape.H)
+        wg = L.router_w("cpu")
+        ids, _, _ = oracle.route(oracle.router_logits(x, wg), shape.k)
+        experts = {}
+        for e in ids.ravel().tolist():
+            g, u, d = L.expert_f32(e)
+            experts[e] = (oracle.pack(g), oracle.pack(u), oracle.pack(d))
+        sg, su, sd = L.shared_f32()
+        shared = (oracle.pack(sg), oracle.pack(su), oracle.pack(sd))
+        sgv = L.shared_sigmoid_w("cpu")
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, wg, sgv, experts, shared, shape.k)
+        times.append(time.perf_counter() - t0)
+        seed += 1
+    us = 1e6 * sum(times) / len(times)
+    return us, len(times), sum(times)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    us, n, tot = cpu_oracle_sample(max(5.0, args.cpu_seconds))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": n, "warmup": 0, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "%d single-token layer calls" % n},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d tokens of the T=1 decode workload (seeds 0..%d), %.1f s of CPU" %
+                                   (n, min(n, N_SEEDS) - 1, tot)},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def build_layers(nv, wl, device, n):
+    shape = wl.QWEN36_35B_A3B
+    layers, xs = [], []
+    for seed in range(n):
+        L = wl.LayerInputs(shape, seed=seed)
+        layer = nv.MoELayer.allocate(shape.H, shape.E, shape.k, shape.I, shape.Is, nv.SCALE_E4M3, device)
+        layer.router_w.copy_(L.router_w(device))
+        for e in range(shape.E):
+            layer.pack_expert(e, *L.expert_f32(e, device=device))
+        layer.pack_shared(*L.shared_f32(device=device), L.shared_sigmoid_w(device))
+        layers.append(layer)
+        xs.append(wl.activations(seed, 1, shape.H, device=device))
+    torch.cuda.synchronize()
+    return layers, xs
+
+
+def step_bytes(layer, ids_row, T=1):
+    """Algorithmic bytes of one layer call: distinct active experts' packed weights,
+    scales and tensor scales, the shared expert, the router, x and y, routing outputs."""
+    H, I, Is = layer.H, layer.I, layer.Is
+    per_expert = layer.weight_bytes_per_expert()
+    distinct = len(set(int(v) for v in ids_row))
+    shared = 2 * Is * H // 2 + 2 * Is * H // 16 + H * Is // 2 + H * Is // 16 + 12 + 2 * H
+    router = layer.E * H * 2
+    acts = 2 * H * T * 2
+    return distinct * per_expert + shared + router + acts
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    global torch
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_w4a16_moe_gb300 as nv
+    import workload as wl
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    layers, xs = build_layers(nv, wl, device, N_SEEDS)
+    T = 1
+    ws = nv.Workspace(nv.moe_layer_workspace_size(layers[0], T), device=device)
+    descs = [l.desc() for l in layers]
+    ys = [torch.empty(T, layers[0].H, dtype=torch.bfloat16, device=device) for _ in range(N_SEEDS)]
+    stream = torch.cuda.current_stream()
+
+    # routing of every instance, for the byte count of each step
+    ids_all = []
+    for i in range(N_SEEDS):
+        _, ids, _ = nv.moe_layer_forward(layers[i], xs[i], ws=ws, want_route=True, desc=descs[i])
+        ids_all.append(ids.cpu().numpy()[0])
+    bytes_per_step = [step_bytes(layers[i], ids_all[i]) for i in range(N_SEEDS)]
+
+    def step(i):
+        j = i % N_SEEDS
+        nv.moe_layer_forward(layers[j], xs[j], ws=ws, y=ys[j], desc=descs[j])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(K):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    us_per_token = 1e3 * ms / (K * world)
+    avg_bytes = sum(bytes_per_step[i % N_SEEDS] for i in range(K)) / K
+    achieved_gbs = avg_bytes / (us_per_token * 1e-6) / 1e9 / world if world else 0.0
+
+    # end to end through the public API with host buffers: pinned x in, y out, every step
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = torch.empty(T, layers[0].H, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(T, layers[0].H, dtype=torch.bfloat16, device=device)
+    for i in range(5):
+        xd.copy_(xh[i % N_SEEDS], non_blocking=True)
+        nv.moe_layer_forward(layers[i % N_SEEDS], xd, ws=ws, y=ys[0], desc=descs[i % N_SEEDS])
+        yh.copy_(ys[0], non_blocking=True)
+    torch.cuda.synchronize()
+    Ke = min(K, 1000)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(Ke):
+        j = i % N_SEEDS
+        xd.copy_(xh[j], non_blocking=True)
+        nv.moe_layer_forward(layers[j], xd, ws=ws, y=ys[0], desc=descs[j])
+        yh.copy_(ys[0], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = 1e3 * e0.elapsed_time(e1) / Ke
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        us, n, tot = cpu_oracle_sample(args.cpu_seconds)
+        cpu = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d single-token layer calls of the same workload (seeds 0..%d), %.1f s" %
+                         (n, min(n, N_SEEDS) - 1, tot)}
+    launches_per_step = nv.LAUNCHES_PER_DECODE_CALL if hasattr(nv, "LAUNCHES_PER_DECODE_CALL") else None
+    line = {
+        "metric": METRIC, "value": us_per_token, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16-act/nvfp4-weight, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
+        "config": {"workload": WORKLOAD, "tokens_per_step": 1,
+                   "l2": "inputs larger than L2: 32 rotating layer instances (%.1f GB)" % (
+                       sum(l.gu_packed.numel() + l.dn_packed.numel() for l in layers) * 1.125 / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "achieved_gbs": achieved_gbs,
+        "pct_of_8tbs": 100.0 * achieved_gbs / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak if peak else None, "peak_kind": peak_kind,
+                     "traffic": None, "bytes_per_launch": avg_bytes,
+                     "kernel": "whole decode step (all launches of one moe_layer_forward)"},
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": 2 * layers[0].H * T,
+                "d2h_bytes_per_step": 2 * layers[0].H * T},
+        "gpu_launches": (launches_per_step * K) if launches_per_step else None,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,148 @@
+// Device-side helpers shared by the sm_103a kernels of the NVFP4 W4A16 MoE
+// library: number-format conversions done with the Blackwell cvt instructions,
+// streaming loads, warp reductions, the workspace header and bounded waits.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4moe.h"
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------- workspace
+// Every workspace starts with this header. `status` holds an nvfp4_status the
+// device recorded; `barrier` counts grid-barrier arrivals monotonically across
+// launches (one 64-bit counter never wraps in practice).
+struct alignas(256) WsHeader {
+    uint32_t status;
+    uint32_t pad0;
+    unsigned long long barrier;
+    unsigned int amax_bits;      // nvfp4_pack: max |w| as fp32 bits
+    unsigned int pad1[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+constexpr uint64_t kDefaultWaitLimit = 20000000ull;  // ~1 s of 32-64 ns sleeps
+
+__device__ __forceinline__ void record_status(WsHeader* h, uint32_t code) {
+    atomicCAS(&h->status, 0u, code);
+}
+
+// ---------------------------------------------------------------- bf16 / f16
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fp32 -> bf16, round to nearest even (finite inputs; NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+
+// Two E2M1 codes (one byte: low nibble = first element) -> two fp32 values.
+// cvt.rn.f16x2.e2m1x2 is exact (every E2M1 value is an f16), and so is f16->f32.
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n .reg .b8 b;\n cvt.u8.u32 b, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(h2) : "r"(byte));
+    float lo, hi;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// E4M3 byte -> fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n .reg .b16 b;\n cvt.u16.u32 b, %1;\n cvt.rn.f16x2.e4m3x2 %0, b;\n}" : "=r"(h2) : "r"(byte & 0xFFu));
+    return f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
+}
+
+// Decoded block scale of block `i` of a scale row (E4M3 bytes or FP16 halves).
+template <int KIND>
+__device__ __forceinline__ float scale_at(const void* row, int i) {
+    if constexpr (KIND == NVFP4_SCALE_E4M3) {
+        return e4m3_to_f32(static_cast<const uint8_t*>(row)[i]);
+    } else {
+        return f16_bits_to_f32(static_cast<const uint16_t*>(row)[i]);
+    }
+}
+
+// ---------------------------------------------------------------- loads
+// Weights are read exactly once per call: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- dot kernels
+// Sum over 32 consecutive NVFP4 elements (16 bytes = one uint4, two scale
+// blocks) against 32 fp32 activations: s0 * sum_{0..15} q x + s1 * sum_{16..31} q x.
+// The per-16 partial is multiplied by its scale in fp32 (exact for E4M3 scales
+// up to rounding of the partial; FP16 scales are handled the same way).
+__device__ __forceinline__ float dot32(const uint4 w, const float* x, float s0, float s1) {
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    float p[2] = {0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float2 v = e2m1x2_to_f32x2(words[q] >> (8 * b));
+            p[q >> 1] = fmaf(v.x, x[8 * q + 2 * b], p[q >> 1]);
+            p[q >> 1] = fmaf(v.y, x[8 * q + 2 * b + 1], p[q >> 1]);
+        }
+    }
+    return fmaf(s0, p[0], s1 * p[1]);
+}
+
+// Dequantise 32 elements (one uint4) into fp32 q-values (scale not applied).
+__device__ __forceinline__ void dequant32(const uint4 w, float* q) {
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float2 v = e2m1x2_to_f32x2(words[i] >> (8 * b));
+            q[i * 8 + 2 * b] = v.x;
+            q[i * 8 + 2 * b + 1] = v.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- misc
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void nanosleep_ns(unsigned ns) { __nanosleep(ns); }
+
+}  // namespace nvfp4

@@ -1,0 +1,51 @@
+// Launchers of the sm_103a kernels (internal; the C ABI in api.cu validates
+// arguments and calls these).
+#pragma once
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+};
+
+cudaError_t launch_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scales,
+                        float* tensor_scale, WsHeader* ws, int num_sms, cudaStream_t s);
+
+cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_t* y,
+                        const DeviceInfo& dev, cudaStream_t s);
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                              cudaStream_t s);
+cudaError_t launch_route_lists(const int32_t* ids, int total, int E, int32_t* offsets,
+                               int32_t* token_list, int32_t* active, cudaStream_t s);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                         int32_t* offsets, int32_t* token_list, cudaStream_t s);
+
+// Workspace of one layer call (device scratch carved from the caller's buffer).
+struct LayerWs {
+    WsHeader* hdr;
+    float* logits;        // [T, E]
+    float* gate_logit;    // [T]        shared-expert sigmoid gate pre-activation
+    int32_t* ids;         // [T, k]
+    float* w;             // [T, k]
+    int32_t* offsets;     // [E + 1]
+    int32_t* token_list;  // [T * k]
+    int32_t* active;      // [E + 1]    active[0] = A, active[1..A] = expert ids ascending
+    float* h;             // [T * k, I] routed SwiGLU intermediates (entry-major)
+    float* hs;            // [T, Is]    shared intermediates
+    size_t bytes;
+};
+
+LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T);
+size_t layer_ws_bytes(const moe_layer_desc& d, int T);
+
+cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
+                              int32_t* ids_out, float* w_out, const LayerWs& ws,
+                              const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
+
+}  // namespace nvfp4

@@ -18,3 +18,14 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def nv():
+    """The CUDA library (built in-tree if needed). GPU tests fail loudly without it."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_w4a16_moe_gb300 as nvmod
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return nvmod

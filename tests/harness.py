@@ -69,3 +69,46 @@ def tol_ok(gpu: np.ndarray, ref: np.ndarray, rel=1e-2, abs_=1e-3):
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_layer(L: wl.LayerInputs, kind=0, device="cuda", with_shared=True):
+    """Device layer in the library's layout, every expert packed on the GPU by nvfp4_pack."""
+    import nvfp4_w4a16_moe_gb300 as nv
+    s = L.shape
+    Is = s.Is if with_shared else 0
+    layer = nv.MoELayer.allocate(s.H, s.E, s.k, s.I, Is, kind, device)
+    layer.router_w.copy_(L.router_w(device))
+    for e in range(s.E):
+        layer.pack_expert(e, *L.expert_f32(e, device=device))
+    if with_shared:
+        layer.pack_shared(*L.shared_f32(device=device), L.shared_sigmoid_w(device))
+    return layer
+
+
+def check_layer_parity(L: wl.LayerInputs, x_gpu, y_gpu, ids_gpu, w_gpu, kind=0, with_shared=True,
+                       cache=None, gap_min=1e-3):
+    """Compare one GPU layer call with the oracle. Tokens whose k-th/(k+1)-th logit gap
+    is <= gap_min are re-evaluated by the oracle on the GPU's expert set (several
+    routings are correct there). Returns (err, bound, n_near_ties)."""
+    x = x_gpu.cpu()
+    ids_g = ids_gpu.cpu().numpy()
+    w_g = w_gpu.cpu().numpy()
+    res, logits = oracle_layer(L, x, kind, cache=cache, with_shared=with_shared)
+    gap = oracle.logit_gap(logits, L.shape.k)
+    near = gap <= gap_min
+    for t in np.flatnonzero(~near):
+        assert sorted(ids_g[t].tolist()) == sorted(res.ids[t].tolist()), (t, ids_g[t], res.ids[t])
+        # weights compared by expert id
+        wo = dict(zip(res.ids[t].tolist(), res.w[t].tolist()))
+        for e, wv in zip(ids_g[t].tolist(), w_g[t].tolist()):
+            assert abs(wv - wo[e]) <= 1e-5, (t, e, wv, wo[e])
+    ref = res.y
+    if near.any():
+        forced = res.ids.copy()
+        forced[near] = ids_g[near]
+        ref2, _ = oracle_layer(L, x, kind, force_ids=forced, cache=cache, with_shared=with_shared)
+        ref = ref2.y
+    got = y_gpu.float().cpu().numpy().astype(np.float64)
+    ok, err, bound = tol_ok(got, ref)
+    assert ok, "max|gpu-oracle| %.4g > %.4g" % (err, bound)
+    return err, bound, int(near.sum())
