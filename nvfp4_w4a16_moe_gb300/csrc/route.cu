@@ -103,7 +103,7 @@ route_lists_kernel(const int32_t* __restrict__ ids, int total, int E,
     }
     __syncthreads();
     for (int base = 0; base < total; base += kListThreads) {
-        for (int i = tid; i < (kListThreads / 32) * E; i += kListThreads) (&wcnt[0][0])[i] = 0;
+        for (int i = tid; i < (kListThreads / 32) * E; i += kListThreads) wcnt[i / E][i % E] = 0;
         __syncthreads();
         const int idx = base + tid;
         const int e = idx < total ? ids[idx] : -1;
