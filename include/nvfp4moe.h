@@ -226,10 +226,10 @@ NVFP4_API nvfp4_status nvfp4_workspace_init(void* workspace, size_t workspace_by
  * clear != 0 the word is reset to NVFP4_OK afterwards. */
 NVFP4_API nvfp4_status nvfp4_get_device_status(void* workspace, int32_t clear, void* stream);
 
-/* Iteration limit of every bounded device wait (0 restores the default,
- * about one second). Tests lower it to make a wait run out on purpose; the
+/* Time limit, in nanoseconds, of every bounded device wait (0 restores the
+ * default of 2 s). Tests lower it to make a wait run out on purpose; the
  * waiting blocks then record NVFP4_ERR_DEVICE_TIMEOUT and return. */
-NVFP4_API void nvfp4_set_device_wait_limit(uint64_t spins);
+NVFP4_API void nvfp4_set_device_wait_limit(uint64_t limit_ns);
 
 NVFP4_API const char* nvfp4_status_string(nvfp4_status s);
 NVFP4_API int32_t nvfp4_version(void);

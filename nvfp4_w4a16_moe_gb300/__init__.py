@@ -24,8 +24,13 @@ LIB_PATH = os.path.join(HERE, "libnvfp4moe.so")
 SCALE_E4M3 = 0
 SCALE_FP16 = 1
 
-# kernel launches one moe_layer_forward decode call enqueues (routing outputs not requested)
-LAUNCHES_PER_DECODE_CALL = 5
+
+def launches_per_layer_call(T: int, H: int = 2048) -> int:
+    """Kernel launches one moe_layer_forward call enqueues (routing outputs not requested):
+    one for the single-token fused kernel, five for the multi-token decode path."""
+    if T == 1 and H % 256 == 0 and H <= 2048:
+        return 1
+    return 5
 
 STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pointer not 16-byte aligned",

@@ -155,6 +155,9 @@ nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32
     if ((st = device_info(&dev)) != NVFP4_OK) return st;
     if (T == 0) return NVFP4_OK;
     LayerWs ws = carve_layer_ws(workspace, *d, T);
+    if (fused_decode_supported(*d, T, dev))
+        return from_cuda(launch_moe_decode_fused(*d, x, y, topk_ids_out, topk_w_out, ws, dev,
+                                                 g_wait_limit.load(), static_cast<cudaStream_t>(stream)));
     return from_cuda(launch_moe_decode(*d, x, T, y, topk_ids_out, topk_w_out, ws, dev,
                                        g_wait_limit.load(), static_cast<cudaStream_t>(stream)));
 }
@@ -179,8 +182,8 @@ nvfp4_status nvfp4_get_device_status(void* workspace, int32_t clear, void* strea
     return static_cast<nvfp4_status>(code);
 }
 
-void nvfp4_set_device_wait_limit(uint64_t spins) {
-    g_wait_limit.store(spins == 0 ? kDefaultWaitLimit : spins);
+void nvfp4_set_device_wait_limit(uint64_t limit_ns) {
+    g_wait_limit.store(limit_ns == 0 ? kDefaultWaitLimit : limit_ns);
 }
 
 const char* nvfp4_status_string(nvfp4_status s) {

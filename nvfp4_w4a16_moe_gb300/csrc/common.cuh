@@ -24,7 +24,14 @@ struct alignas(256) WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
-constexpr uint64_t kDefaultWaitLimit = 20000000ull;  // ~1 s of 32-64 ns sleeps
+// Every device-side wait is bounded in time (nanoseconds of %globaltimer).
+constexpr uint64_t kDefaultWaitLimit = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ void record_status(WsHeader* h, uint32_t code) {
     atomicCAS(&h->status, 0u, code);
@@ -140,9 +147,67 @@ __device__ __forceinline__ void dequant32(const uint4 w, float* q) {
 }
 
 // ---------------------------------------------------------------- misc
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
-__device__ __forceinline__ float sigmoid_f32(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f32(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void nanosleep_ns(unsigned ns) { __nanosleep(ns); }
+
+}  // namespace nvfp4
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------- TMA bulk copies + mbarriers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// make mbarrier initialisation visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// Bring the first floor16(bytes) bytes at p (16-byte aligned) into L2; a prefetch
+// never touches memory past the buffer.
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t* p, size_t bytes) {
+    const size_t n = bytes & ~size_t(15);
+    for (size_t o = 0; o < n; o += (1u << 20)) {
+        const uint32_t len = (uint32_t)(n - o < (1u << 20) ? n - o : (1u << 20));
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p + o), "r"(len) : "memory");
+    }
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier for at most `limit_ns`; false if it ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
 
 }  // namespace nvfp4

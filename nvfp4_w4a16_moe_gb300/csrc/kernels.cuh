@@ -38,6 +38,7 @@ struct LayerWs {
     int32_t* active;      // [E + 1]    active[0] = A, active[1..A] = expert ids ascending
     float* h;             // [T * k, I] routed SwiGLU intermediates (entry-major)
     float* hs;            // [T, Is]    shared intermediates
+    unsigned long long* words;  // [E + 2 + k*I + Is] (launch tag, value) words of the one-launch kernel
     size_t bytes;
 };
 
@@ -47,5 +48,11 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T);
 cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                               int32_t* ids_out, float* w_out, const LayerWs& ws,
                               const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
+
+// One-launch single-token decode (persistent grid, two bounded grid barriers).
+bool fused_decode_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev);
+cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, uint16_t* y,
+                                    int32_t* ids_out, float* w_out, const LayerWs& ws,
+                                    const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
 
 }  // namespace nvfp4

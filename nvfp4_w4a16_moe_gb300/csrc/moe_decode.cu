@@ -354,6 +354,7 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T) {
     b += align256(sizeof(int32_t) * (size_t)(d.E + 1));
     b += align256(sizeof(float) * Tk * d.I);
     b += align256(sizeof(float) * (size_t)T * d.Is);
+    b += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
     return b;
 }
 
@@ -371,6 +372,8 @@ LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T) {
     w.active = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * (size_t)(d.E + 1));
     w.h = reinterpret_cast<float*>(p); p += align256(sizeof(float) * Tk * d.I);
     w.hs = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (size_t)T * d.Is);
+    w.words = reinterpret_cast<unsigned long long*>(p);
+    p += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
     w.bytes = (size_t)(p - static_cast<char*>(base));
     return w;
 }
