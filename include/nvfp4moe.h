@@ -217,6 +217,30 @@ NVFP4_API nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t
                                size_t workspace_bytes, void* stream);
 NVFP4_API size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T);
 
+/*
+ * moe_layer_forward_noalloc - the same layer as moe_layer_forward, for callers
+ * that cannot allocate device memory where they run the layer (a host callback,
+ * a plugin whose host framework owns all device allocations, a process whose
+ * memory budget is fixed up front). The pages have no counterpart to this call:
+ * it only changes where the scratch lives.
+ *   Arguments as for moe_layer_forward, without the workspace. The scratch is a
+ *   static 4 MiB device array inside this library; every GPU that loads the
+ *   library keeps it reserved until the process exits. Nothing is allocated:
+ *   no cudaMalloc, cudaFree or allocating library routine is called.
+ *   The first call on a device looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current); make that first call
+ *   before any stream capture. Each call clears the part of the array it uses
+ *   (an asynchronous memset on `stream`) and then runs the layer.
+ *   All calls on a device share the one array: calls that can overlap on the
+ *   GPU (different streams without ordering) race and must not be made.
+ *   A layer whose scratch (moe_layer_workspace_size) exceeds 4 MiB is rejected
+ *   with NVFP4_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. Device-side
+ *   wait timeouts are recorded in the array but cannot be read back.
+ */
+NVFP4_API nvfp4_status moe_layer_forward_noalloc(const moe_layer_desc* d, const uint16_t* x, int32_t T,
+                                                 uint16_t* y, int32_t* topk_ids_out, float* topk_w_out,
+                                                 void* stream);
+
 /* Zero a workspace (enqueued on `stream`). Needed once before first use, and
  * again after a call reported NVFP4_ERR_DEVICE_TIMEOUT. */
 NVFP4_API nvfp4_status nvfp4_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

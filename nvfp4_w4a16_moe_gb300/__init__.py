@@ -100,6 +100,8 @@ lib.nvfp4_status_string.restype = ctypes.c_char_p
 lib.nvfp4_status_string.argtypes = [_i32]
 lib.nvfp4_version.restype = _i32
 lib.nvfp4_version.argtypes = []
+lib.moe_layer_forward_noalloc.restype = _i32
+lib.moe_layer_forward_noalloc.argtypes = [ctypes.POINTER(MoELayerDescC), _P, _i32, _P, _P, _P, _P]
 
 
 def _check(status: int, where: str):
@@ -332,6 +334,26 @@ def moe_layer_forward(layer: MoELayer, x: torch.Tensor, ws: Optional[Workspace] 
         w_out = torch.empty(T, layer.k, dtype=torch.float32, device=x.device)
     _check(lib.moe_layer_forward(ctypes.byref(d), _ptr(x), T, _ptr(y), _ptr(ids_out), _ptr(w_out),
                                  ws.ptr(), ws.nbytes, _stream(stream)), "moe_layer_forward")
+    if want_route:
+        return y, ids_out, w_out
+    return y
+
+
+def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, y: Optional[torch.Tensor] = None,
+                              ids_out: Optional[torch.Tensor] = None, w_out: Optional[torch.Tensor] = None,
+                              want_route: bool = False, stream=None):
+    """moe_layer_forward with the library's static scratch instead of a workspace
+    (for callers that cannot allocate device memory where they run the layer)."""
+    x = _u16(x)
+    T = x.shape[0]
+    d = layer.desc()
+    if y is None:
+        y = torch.empty(T, layer.H, dtype=torch.bfloat16, device=x.device)
+    if want_route and ids_out is None:
+        ids_out = torch.empty(T, layer.k, dtype=torch.int32, device=x.device)
+        w_out = torch.empty(T, layer.k, dtype=torch.float32, device=x.device)
+    _check(lib.moe_layer_forward_noalloc(ctypes.byref(d), _ptr(x), T, _ptr(y), _ptr(ids_out), _ptr(w_out),
+                                         _stream(stream)), "moe_layer_forward_noalloc")
     if want_route:
         return y, ids_out, w_out
     return y

@@ -1,0 +1,56 @@
+"""moe_layer_forward_noalloc: the layer with the library's static scratch array
+instead of a caller workspace, for callers that cannot allocate device memory
+where they run the layer. Checked through the C ABI against moe_layer_forward
+on the same inputs, two calls in a row, for the one-launch single-token path
+and the multi-token path. This file is collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workload as wl
+from harness import gpu_layer, tol_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(nv, layer, x):
+    d = layer.desc()
+    T = x.shape[0]
+    y = torch.empty(T, layer.H, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(T, layer.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, layer.k, dtype=torch.float32, device="cuda")
+    st = nv.lib.moe_layer_forward_noalloc(ctypes.byref(d), ctypes.c_void_p(x.data_ptr()), T,
+                                          ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(ids.data_ptr()),
+                                          ctypes.c_void_p(w.data_ptr()), nv._stream())
+    assert st == nv.NVFP4_OK, st
+    return y, ids, w
+
+
+@pytest.mark.parametrize("shape,T", [(wl.TINY, 1), (wl.TINY, 5), (wl.QWEN36_35B_A3B, 1)])
+def test_noalloc_matches_workspace_entry_point(nv, shape, T):
+    L = wl.LayerInputs(shape, seed=7)
+    layer = gpu_layer(L)
+    x = wl.activations(7, T, shape.H).cuda()
+    y_ref, ids_ref, w_ref = nv.moe_layer_forward(layer, x, want_route=True)
+    for _ in range(2):   # two calls in a row share the static scratch
+        y, ids, w = _noalloc(nv, layer, x)
+        torch.cuda.synchronize()
+        ok, err, bound = tol_ok(y.float().cpu().numpy().astype(np.float64),
+                                y_ref.float().cpu().numpy().astype(np.float64))
+        assert ok, (err, bound)
+        assert torch.equal(ids, ids_ref)
+        assert torch.allclose(w, w_ref, atol=1e-6)
+
+
+def test_noalloc_rejects_oversized_scratch(nv):
+    L = wl.LayerInputs(wl.QWEN36_35B_A3B, seed=0)
+    layer = gpu_layer(L)
+    x = torch.zeros(64, 2048, dtype=torch.bfloat16, device="cuda")
+    d = layer.desc()
+    d.E, d.k, d.I, d.Is = 256, 8, 8192, 8192    # 64 tokens x 8 x 8192 intermediates: far above 4 MiB
+    y = torch.empty(64, 2048, dtype=torch.bfloat16, device="cuda")
+    st = nv.lib.moe_layer_forward_noalloc(ctypes.byref(d), ctypes.c_void_p(x.data_ptr()), 64,
+                                          ctypes.c_void_p(y.data_ptr()), None, None, nv._stream())
+    assert st == nv.NVFP4_ERR_WORKSPACE_TOO_SMALL
