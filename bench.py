@@ -49,6 +49,20 @@ def dist_env():
     return rank, world, local
 
 
+def ncu_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu capture, or
+    None when the kernel source changed since that capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "moe_decode_t1_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = open(os.path.join(ROOT, d["source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != d["source_sha256_prefix"]:
+        return None
+    return d["dram_bytes_read"] + d["dram_bytes_write"]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -336,7 +350,7 @@ def main():
         "pct_of_8tbs": 100.0 * achieved_gbs / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak if peak else None, "peak_kind": peak_kind,
-                     "traffic": None, "bytes_per_launch": avg_bytes,
+                     "traffic": ncu_traffic(), "bytes_per_launch": avg_bytes,
                      "kernel": "moe_decode_t1_kernel (the whole step is this one launch)"},
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": 2 * layers[0].H * T,
                 "d2h_bytes_per_step": 2 * layers[0].H * T},
