@@ -135,6 +135,7 @@ typedef struct {
 #define NVFP4_MAX_GEMV_TOKENS 64  /* nvfp4_gemv_w4a16: 1 <= T <= 64            */
 #define NVFP4_DECODE_MAX_TOKENS 64 /* moe_layer_forward: T <= 64 decode path,  */
                                    /* larger T takes the prefill path          */
+#define NVFP4_MAX_TOKENS 65536     /* moe_layer_forward / workspace_size: T cap */
 
 /*
  * nvfp4_pack - quantise an fp32 matrix to NVFP4.
@@ -209,8 +210,13 @@ NVFP4_API nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E,
  *                 (it carries a barrier counter across calls); calls that share
  *                 a workspace must be serialised on one stream.
  *   Shapes: H % 32 == 0, I % 32 == 0, Is % 32 == 0 (or Is == 0), 1 <= k <= 8,
- *   k <= E <= 256, 0 <= T. T <= 64 runs the one-launch decode kernel, larger
- *   T the grouped prefill path.
+ *   k <= E <= 256, 0 <= T <= 65536.
+ *   Paths: T == 1 runs the one-launch decode kernel (H % 256 == 0, H <= 2048,
+ *   k*I + Is <= 8192; otherwise the multi-token path), 2 <= T <= 64 the
+ *   multi-token decode kernels, T > 64 with E4M3 scales the grouped prefill path
+ *   (tensor-core GEMMs with the weights dequantised to bf16 in shared memory;
+ *   the SwiGLU intermediate is rounded to bf16 there, the activation type).
+ *   T > 64 with FP16 scales runs as 64-token chunks of the multi-token path.
  */
 NVFP4_API nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32_t T, uint16_t* y,
                                int32_t* topk_ids_out, float* topk_w_out, void* workspace,

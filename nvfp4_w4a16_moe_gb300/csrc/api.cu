@@ -39,6 +39,14 @@ nvfp4_status device_info(DeviceInfo* out) {
     return NVFP4_OK;
 }
 
+// Scratch bytes of one moe_layer_forward call: the prefill path's for T > 64 with
+// E4M3 scales; FP16-scaled layers run T > 64 as 64-token chunks of the decode path.
+size_t layer_bytes(const moe_layer_desc& d, int T) {
+    if (T > NVFP4_DECODE_MAX_TOKENS)
+        return prefill_supported(d, T) ? prefill_ws_bytes(d, T) : layer_ws_bytes(d, NVFP4_DECODE_MAX_TOKENS);
+    return layer_ws_bytes(d, T);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
@@ -134,8 +142,8 @@ nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k
 }
 
 size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T) {
-    if (!d || T < 0) return 0;
-    return layer_ws_bytes(*d, T);
+    if (!d || T < 0 || T > NVFP4_MAX_TOKENS) return 0;
+    return layer_bytes(*d, T);
 }
 
 nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32_t T, uint16_t* y,
@@ -143,23 +151,39 @@ nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32
                                size_t workspace_bytes, void* stream) {
     nvfp4_status st = check_layer(d);
     if (st != NVFP4_OK) return st;
-    if (T < 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (T > NVFP4_DECODE_MAX_TOKENS) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // prefill path: not yet
+    if (T < 0 || T > NVFP4_MAX_TOKENS) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (T > 0 && (!x || !y)) return NVFP4_ERR_INVALID_ARG;
     if (!workspace) return NVFP4_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (y && !aligned16(y)) || !aligned16(workspace) ||
         (topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
         return NVFP4_ERR_MISALIGNED;
-    if (workspace_bytes < layer_ws_bytes(*d, T)) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace_bytes < layer_bytes(*d, T)) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     DeviceInfo dev;
     if ((st = device_info(&dev)) != NVFP4_OK) return st;
     if (T == 0) return NVFP4_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > NVFP4_DECODE_MAX_TOKENS) {
+        if (prefill_supported(*d, T)) {
+            PrefillWs pws = carve_prefill_ws(workspace, *d, T);
+            return from_cuda(launch_moe_prefill(*d, x, T, y, topk_ids_out, topk_w_out, pws, s));
+        }
+        LayerWs cws = carve_layer_ws(workspace, *d, NVFP4_DECODE_MAX_TOKENS);
+        for (int t0 = 0; t0 < T; t0 += NVFP4_DECODE_MAX_TOKENS) {
+            const int tc = T - t0 < NVFP4_DECODE_MAX_TOKENS ? T - t0 : NVFP4_DECODE_MAX_TOKENS;
+            const size_t xo = (size_t)t0 * d->H, ko = (size_t)t0 * d->k;
+            cudaError_t e = launch_moe_decode(*d, x + xo, tc, y + xo, topk_ids_out ? topk_ids_out + ko : nullptr,
+                                              topk_w_out ? topk_w_out + ko : nullptr, cws, dev,
+                                              g_wait_limit.load(), s);
+            if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        }
+        return NVFP4_OK;
+    }
     LayerWs ws = carve_layer_ws(workspace, *d, T);
     if (fused_decode_supported(*d, T, dev))
         return from_cuda(launch_moe_decode_fused(*d, x, y, topk_ids_out, topk_w_out, ws, dev,
-                                                 g_wait_limit.load(), static_cast<cudaStream_t>(stream)));
+                                                 g_wait_limit.load(), s));
     return from_cuda(launch_moe_decode(*d, x, T, y, topk_ids_out, topk_w_out, ws, dev,
-                                       g_wait_limit.load(), static_cast<cudaStream_t>(stream)));
+                                       g_wait_limit.load(), s));
 }
 
 nvfp4_status nvfp4_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

@@ -55,4 +55,28 @@ cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, 
                                     int32_t* ids_out, float* w_out, const LayerWs& ws,
                                     const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
 
+// Prefill path (T > 64 tokens, E4M3 scales): grouped tensor-core GEMMs.
+struct PrefillWs {
+    WsHeader* hdr;
+    float* logits;        // [T, E]
+    float* gate;          // [T]
+    int32_t* ids;         // [T, k]
+    float* w;             // [T, k]
+    int32_t* bcount;      // [ceil(T*k / 1024), E]  per-block counts, then bases
+    int32_t* offsets;     // [E + 1]
+    int32_t* mt_prefix;   // [E + 2]  first 128-row tile of each slot (E = shared)
+    int32_t* token_list;  // [T * k]
+    uint16_t* h;          // [T * k, I]  bf16 SwiGLU intermediates, token_list order
+    uint16_t* hs;         // [T, Is]     bf16 shared intermediates
+    float* Y;             // [T, k + 1, H] weighted expert outputs
+    size_t bytes;
+};
+
+bool prefill_supported(const moe_layer_desc& d, int T);
+size_t prefill_ws_bytes(const moe_layer_desc& d, int T);
+PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T);
+int prefill_launch_count(const moe_layer_desc& d);
+cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
+                               int32_t* ids_out, float* w_out, const PrefillWs& ws, cudaStream_t s);
+
 }  // namespace nvfp4

@@ -1,0 +1,135 @@
+"""moe_layer_forward on the prefill path (T > 64 tokens) against the oracle.
+
+The layer is the same as on the decode path (lynn-engine tutorials index, row
+06; lynn-engine README, P28/P29 notes) computed as grouped tensor-core GEMMs
+(lynn-engine README, P2/P3-A notes). Bar as for decode: max|gpu - oracle| <=
+1e-2 * max|oracle| + 1e-3 per output tensor; expert ids exact as sets and
+weights within 1e-5 for every token whose k-th/(k+1)-th logit gap exceeds 1e-3.
+The layer treats tokens independently, so at full size the oracle is evaluated
+on a sample of tokens (x rows picked out) and compared with the same rows of the
+GPU output; routing is checked on every token.
+"""
+import json
+import os
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload as wl
+from harness import check_layer_parity, gpu_layer, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+QW = wl.QWEN36_35B_A3B
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "prefill_zipf.json")
+
+
+def _forward(nv, layer, x):
+    y, ids, w = nv.moe_layer_forward(layer, x.cuda(), want_route=True)
+    torch.cuda.synchronize()
+    return y, ids, w
+
+
+def _check_routing_all(L, x, ids_gpu, w_gpu, gap_min=1e-3):
+    """Routing of every token against the oracle's fp64 router."""
+    logits = oracle.router_logits(x, L.router_w("cpu"))
+    ids_o, w_o, _ = oracle.route(logits, L.shape.k)
+    gap = oracle.logit_gap(logits, L.shape.k)
+    ids_g = ids_gpu.cpu().numpy()
+    w_g = w_gpu.cpu().numpy()
+    clear = gap > gap_min
+    assert np.array_equal(np.sort(ids_g[clear], 1), np.sort(ids_o[clear], 1))
+    for t in np.flatnonzero(clear):
+        wo = dict(zip(ids_o[t].tolist(), w_o[t].tolist()))
+        for e, wv in zip(ids_g[t].tolist(), w_g[t].tolist()):
+            assert abs(wv - wo[e]) <= 1e-5, (t, e, wv, wo[e])
+    return ids_o
+
+
+def _sampled_parity(L, x, y, ids, w, rows, kind=0):
+    rows = sorted(set(int(r) for r in rows))
+    idx = torch.tensor(rows, dtype=torch.long)
+    return check_layer_parity(L, x[idx], y.cpu()[idx], ids.cpu()[idx], w.cpu()[idx], kind=kind)
+
+
+@pytest.mark.parametrize("T", [65, 200, 777])
+def test_tiny_prefill(nv, T):
+    """Every token of a small layer: several 128-row tiles per expert and ragged tails."""
+    L = wl.LayerInputs(wl.TINY, seed=100 + T)
+    layer = gpu_layer(L)
+    x = wl.activations(100 + T, T, wl.TINY.H)
+    y, ids, w = _forward(nv, layer, x)
+    check_layer_parity(L, x, y, ids, w)
+
+
+def test_tiny_prefill_no_shared_expert(nv):
+    L = wl.LayerInputs(wl.TINY, seed=7)
+    layer = gpu_layer(L, with_shared=False)
+    x = wl.activations(7, 300, wl.TINY.H)
+    y, ids, w = _forward(nv, layer, x)
+    check_layer_parity(L, x, y, ids, w, with_shared=False)
+
+
+def test_tiny_prefill_skewed_routing(nv):
+    """Strongly skewed router: some experts get no tokens, others several tiles."""
+    shape = replace(wl.TINY, router_kappa=1.5)
+    L = wl.LayerInputs(shape, seed=11)
+    layer = gpu_layer(L)
+    x = wl.activations(11, 1000, shape.H)
+    y, ids, w = _forward(nv, layer, x)
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=shape.E)
+    assert counts.max() > 256
+    check_layer_parity(L, x, y, ids, w)
+
+
+def test_tiny_prefill_fp16_scales(nv):
+    """FP16-scaled layers above 64 tokens run as 64-token chunks of the decode path."""
+    L = wl.LayerInputs(wl.TINY, seed=5)
+    layer = gpu_layer(L, kind=1)
+    x = wl.activations(5, 150, wl.TINY.H)
+    y, ids, w = _forward(nv, layer, x)
+    check_layer_parity(L, x, y, ids, w, kind=1)
+
+
+def test_prefill_deterministic(nv):
+    L = wl.LayerInputs(wl.TINY, seed=3)
+    layer = gpu_layer(L)
+    x = wl.activations(3, 500, wl.TINY.H).cuda()
+    y1 = nv.moe_layer_forward(layer, x)
+    y2 = nv.moe_layer_forward(layer, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_qwen_prefill_300_sampled(nv):
+    L = wl.LayerInputs(QW, seed=4)
+    layer = gpu_layer(L)
+    T = 300
+    x = wl.activations(4, T, QW.H)
+    y, ids, w = _forward(nv, layer, x)
+    _check_routing_all(L, x, ids, w)
+    _sampled_parity(L, x, y, ids, w, [0, 1, 127, 128, 255, 256, 298, 299])
+
+
+def test_qwen_prefill_4096_zipf(nv):
+    """The 4096-token prefill workload with the skewed router (kappa from the
+    golden calibration): per-expert counts must match the calibration exactly
+    on every token with a clear routing margin; output parity on sampled tokens."""
+    with open(GOLDEN) as f:
+        gold = json.load(f)
+    shape = replace(QW, router_kappa=gold["kappa"])
+    L = wl.LayerInputs(shape, seed=gold["seed"])
+    layer = gpu_layer(L)
+    T = gold["T"]
+    x = wl.activations(gold["seed"], T, shape.H)
+    y, ids, w = _forward(nv, layer, x)
+    ids_o = _check_routing_all(L, x, ids, w)
+    assert np.array_equal(np.bincount(ids_o.ravel(), minlength=shape.E), np.array(gold["counts"]))
+    g = np.bincount(ids.cpu().numpy().ravel(), minlength=shape.E)
+    assert abs(int(g.max()) - gold["max_count"]) <= 8
+    rng = np.random.default_rng(0)
+    rows = [0, T - 1] + rng.choice(T, 10, replace=False).tolist()
+    _sampled_parity(L, x, y, ids, w, rows)
