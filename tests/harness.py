@@ -86,10 +86,11 @@ def gpu_layer(L: wl.LayerInputs, kind=0, device="cuda", with_shared=True):
 
 
 def check_layer_parity(L: wl.LayerInputs, x_gpu, y_gpu, ids_gpu, w_gpu, kind=0, with_shared=True,
-                       cache=None, gap_min=1e-3):
+                       cache=None, gap_min=1e-3, rel_only=None):
     """Compare one GPU layer call with the oracle. Tokens whose k-th/(k+1)-th logit gap
     is <= gap_min are re-evaluated by the oracle on the GPU's expert set (several
-    routings are correct there). Returns (err, bound, n_near_ties)."""
+    routings are correct there). With ``rel_only`` the error must also stay within
+    rel_only * max|oracle| (no absolute term). Returns (err, bound, n_near_ties)."""
     x = x_gpu.cpu()
     ids_g = ids_gpu.cpu().numpy()
     w_g = w_gpu.cpu().numpy()
@@ -111,4 +112,7 @@ def check_layer_parity(L: wl.LayerInputs, x_gpu, y_gpu, ids_gpu, w_gpu, kind=0, 
     got = y_gpu.float().cpu().numpy().astype(np.float64)
     ok, err, bound = tol_ok(got, ref)
     assert ok, "max|gpu-oracle| %.4g > %.4g" % (err, bound)
+    if rel_only is not None:
+        ok2, err2, bound2 = tol_ok(got, ref, rel=rel_only, abs_=0.0)
+        assert ok2, "max|gpu-oracle| %.4g > %.4g (scale-free)" % (err2, bound2)
     return err, bound, int(near.sum())
