@@ -213,10 +213,11 @@ NVFP4_API nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E,
  *   k <= E <= 256, 0 <= T <= 65536.
  *   Paths: T == 1 runs the one-launch decode kernel (H % 256 == 0, H <= 2048,
  *   k*I + Is <= 8192; otherwise the multi-token path), 2 <= T <= 64 the
- *   multi-token decode kernels, T > 64 with E4M3 scales the grouped prefill path
- *   (tensor-core GEMMs with the weights dequantised to bf16 in shared memory;
- *   the SwiGLU intermediate is rounded to bf16 there, the activation type).
- *   T > 64 with FP16 scales runs as 64-token chunks of the multi-token path.
+ *   multi-token decode kernels, T > 64 with E4M3 scales and H, I, Is multiples
+ *   of 64 the grouped prefill path (tcgen05 tensor-core GEMMs with the weights
+ *   expanded to bf16 in shared memory; the SwiGLU intermediate is rounded to
+ *   bf16 there, the activation type). Other layers with T > 64 run as 64-token
+ *   chunks of the multi-token path.
  */
 NVFP4_API nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32_t T, uint16_t* y,
                                int32_t* topk_ids_out, float* topk_w_out, void* workspace,

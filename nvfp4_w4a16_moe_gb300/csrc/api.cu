@@ -165,7 +165,7 @@ nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32
     if (T > NVFP4_DECODE_MAX_TOKENS) {
         if (prefill_supported(*d, T)) {
             PrefillWs pws = carve_prefill_ws(workspace, *d, T);
-            return from_cuda(launch_moe_prefill(*d, x, T, y, topk_ids_out, topk_w_out, pws, s));
+            return from_cuda(launch_moe_prefill(*d, x, T, y, topk_ids_out, topk_w_out, pws, g_wait_limit.load(), s));
         }
         LayerWs cws = carve_layer_ws(workspace, *d, NVFP4_DECODE_MAX_TOKENS);
         for (int t0 = 0; t0 < T; t0 += NVFP4_DECODE_MAX_TOKENS) {

@@ -56,6 +56,29 @@ cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, 
                                     const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
 
 // Prefill path (T > 64 tokens, E4M3 scales): grouped tensor-core GEMMs.
+constexpr int kTokTile = 256;   // token rows per grouped-GEMM tile
+
+// Everything the two grouped GEMMs read. Slots 0..E-1 are the routed experts
+// (rows = their entries in token_list order), slot E the shared expert (rows =
+// tokens 0..T-1). tile_prefix[s] is the first kTokTile-row tile of slot s.
+struct GroupedParams {
+    const uint16_t* x;
+    int T, H, E, k, I, Is;
+    const uint8_t* gu_packed; const uint8_t* gu_scales; const float* gu_tscale;
+    const uint8_t* dn_packed; const uint8_t* dn_scales; const float* dn_tscale;
+    const uint8_t* sh_gu_packed; const uint8_t* sh_gu_scales; const float* sh_gu_tscale;
+    const uint8_t* sh_dn_packed; const uint8_t* sh_dn_scales; const float* sh_dn_tscale;
+    const int32_t* offsets;     // [E + 1]
+    const int32_t* token_list;  // [T * k] entries t*k + j grouped by expert
+    const int32_t* tile_prefix; // [E + 2]
+    const float* w;             // [T, k] routing weights
+    const float* gate;          // [T] shared gate pre-activation
+    uint16_t* h;                // [T * k, I] bf16, rows in token_list order
+    uint16_t* hs;               // [T, Is] bf16
+    float* Y;                   // [T, k + 1, H] fp32 scaled expert outputs
+};
+
+
 struct PrefillWs {
     WsHeader* hdr;
     float* logits;        // [T, E]
@@ -64,7 +87,7 @@ struct PrefillWs {
     float* w;             // [T, k]
     int32_t* bcount;      // [ceil(T*k / 1024), E]  per-block counts, then bases
     int32_t* offsets;     // [E + 1]
-    int32_t* mt_prefix;   // [E + 2]  first 128-row tile of each slot (E = shared)
+    int32_t* tile_prefix; // [E + 2]  first kTokTile-row tile of each slot (E = shared)
     int32_t* token_list;  // [T * k]
     uint16_t* h;          // [T * k, I]  bf16 SwiGLU intermediates, token_list order
     uint16_t* hs;         // [T, Is]     bf16 shared intermediates
@@ -77,6 +100,11 @@ size_t prefill_ws_bytes(const moe_layer_desc& d, int T);
 PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T);
 int prefill_launch_count(const moe_layer_desc& d);
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
-                               int32_t* ids_out, float* w_out, const PrefillWs& ws, cudaStream_t s);
+                               int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
+                               cudaStream_t s);
+// Grouped tcgen05 GEMM over the token tiles of every slot: mode 0 = gate/up with the
+// SwiGLU epilogue (x -> h, hs), mode 1 = down with the weighted epilogue (h, hs -> Y).
+cudaError_t launch_grouped_tc(const GroupedParams& P, int mode, int tiles_max, WsHeader* hdr,
+                              uint64_t wait_limit, cudaStream_t s);
 
 }  // namespace nvfp4

@@ -252,12 +252,12 @@ __global__ void __launch_bounds__(kLB) lists_hist_kernel(const int32_t* __restri
 }
 
 //    pass 2 (one block): bases of every (expert, block) in expert-major order, the
-//    per-expert offsets, and the prefix of 128-row tiles per slot (E experts, then the
-//    shared expert with T rows) used to schedule the grouped GEMMs
+//    per-expert offsets, and the prefix of kTokTile-row tiles per slot (E experts, then
+//    the shared expert with T rows) used to schedule the grouped GEMMs
 __global__ void __launch_bounds__(NVFP4_MAX_EXPERTS) lists_scan_kernel(int32_t* __restrict__ bcount, int nblocks,
                                                                       int E, int shared_rows,
                                                                       int32_t* __restrict__ offsets,
-                                                                      int32_t* __restrict__ mt_prefix) {
+                                                                      int32_t* __restrict__ tile_prefix) {
     __shared__ int tot[NVFP4_MAX_EXPERTS];
     const int e = threadIdx.x;
     int s = 0;
@@ -274,13 +274,13 @@ __global__ void __launch_bounds__(NVFP4_MAX_EXPERTS) lists_scan_kernel(int32_t* 
         int run = 0, mt = 0;
         for (int x = 0; x < E; ++x) {
             offsets[x] = run;
-            mt_prefix[x] = mt;
+            tile_prefix[x] = mt;
             run += tot[x];
-            mt += (tot[x] + kBM - 1) / kBM;
+            mt += (tot[x] + kTokTile - 1) / kTokTile;
         }
         offsets[E] = run;
-        mt_prefix[E] = mt;
-        mt_prefix[E + 1] = mt + (shared_rows + kBM - 1) / kBM;   // the shared expert: every token
+        tile_prefix[E] = mt;
+        tile_prefix[E + 1] = mt + (shared_rows + kTokTile - 1) / kTokTile;   // the shared expert: every token
     }
     __syncthreads();
     if (e < E) {
@@ -319,183 +319,10 @@ __global__ void __launch_bounds__(kLB) lists_place_kernel(const int32_t* __restr
     }
 }
 
-// Slot of a tile: the largest s with mt_prefix[s] <= mt (binary search over E + 2 entries).
-__device__ __forceinline__ int slot_of_tile(const int32_t* mt_prefix, int nslots, int mt) {
-    int lo = 0, hi = nslots;   // mt_prefix[0] = 0 <= mt < mt_prefix[nslots]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (mt_prefix[mid] <= mt) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-// Everything the two grouped GEMMs read. Slots 0..E-1 are the routed experts
-// (rows = their entries in token_list order), slot E the shared expert (rows =
-// tokens 0..T-1). mt_prefix[s] is the first 128-row tile of slot s.
-struct GroupedParams {
-    const uint16_t* x;
-    int T, H, E, k, I, Is;
-    const uint8_t* gu_packed; const uint8_t* gu_scales; const float* gu_tscale;
-    const uint8_t* dn_packed; const uint8_t* dn_scales; const float* dn_tscale;
-    const uint8_t* sh_gu_packed; const uint8_t* sh_gu_scales; const float* sh_gu_tscale;
-    const uint8_t* sh_dn_packed; const uint8_t* sh_dn_scales; const float* sh_dn_tscale;
-    const int32_t* offsets;     // [E + 1]
-    const int32_t* token_list;  // [T * k] entries t*k + j grouped by expert
-    const int32_t* mt_prefix;   // [E + 2]
-    const float* w;             // [T, k] routing weights
-    const float* gate;          // [T] shared gate pre-activation
-    uint16_t* h;                // [T * k, I] bf16, rows in token_list order
-    uint16_t* hs;               // [T, Is] bf16
-    float* Y;                   // [T, k + 1, H] fp32 scaled expert outputs
-};
-
-struct TileRows {
-    int slot, p0, n_rows;   // slot, first row of the tile inside its slot's row space, rows used
-};
-
-__device__ __forceinline__ bool locate_tile(const GroupedParams& P, int mt, TileRows* tr) {
-    const int nslots = P.E + 1;
-    if (mt >= __ldg(P.mt_prefix + nslots)) return false;
-    const int s = slot_of_tile(P.mt_prefix, nslots, mt);
-    const int lm = mt - __ldg(P.mt_prefix + s);
-    tr->slot = s;
-    if (s < P.E) {
-        tr->p0 = __ldg(P.offsets + s) + lm * kBM;
-        tr->n_rows = min(kBM, __ldg(P.offsets + s + 1) - tr->p0);
-    } else {
-        tr->p0 = lm * kBM;
-        tr->n_rows = min(kBM, P.T - tr->p0);
-    }
-    return true;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-
-// 4. gate/up GEMM with the SwiGLU epilogue. Tile (mt, nt): 128 rows of slot s x 64
-//    intermediate indices i0 = 64 nt .. i0 + 63, as 128 B rows: warp column wn owns
-//    intermediates i0 + 16 wn .. + 15, its n8 tiles 0/1 hold their gate rows and 2/3
-//    the matching up rows, so gate and up of one index meet in the same thread.
-//    grid = mt_max * ceil(max(I, Is) / 64); blocks past the last tile return.
-__global__ void __launch_bounds__(kGThreads, 2) grouped_gateup_kernel(const GroupedParams P, int n_tiles) {
-    __shared__ __align__(128) uint16_t sm[4 * kBM * kLds];
-    const int nt = blockIdx.x % n_tiles, mt = blockIdx.x / n_tiles;
-    TileRows tr;
-    if (!locate_tile(P, mt, &tr)) return;
-    const bool shared = tr.slot == P.E;
-    const int Ir = shared ? P.Is : P.I;
-    const int i0 = nt * 64;
-    if (i0 >= Ir) return;
-    const int tid = threadIdx.x, H = P.H;
-
-    TileSrc S{};
-    S.dummy = P.x;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        const int r = (tid >> 2) + 64 * c;
-        if (r < tr.n_rows) {
-            const int tok = shared ? tr.p0 + r : __ldg(P.token_list + tr.p0 + r) / P.k;
-            S.a[c] = P.x + (size_t)tok * H;
-        }
-    }
-    {
-        const int bn = tid >> 1, wn = bn >> 5, rr = bn & 31, jj = rr >> 3;
-        const int ii = i0 + wn * 16 + (jj & 1) * 8 + (rr & 7);
-        if (ii < Ir) {
-            const size_t row = (size_t)(jj < 2 ? ii : Ir + ii);
-            const uint8_t* pk = shared ? P.sh_gu_packed : P.gu_packed + (size_t)tr.slot * 2 * P.I * (H / 2);
-            const uint8_t* sc = shared ? P.sh_gu_scales : P.gu_scales + (size_t)tr.slot * 2 * P.I * (H / 16);
-            S.bq = pk + row * (H / 2);
-            S.bs = sc + row * (H / 16);
-        }
-    }
-    float acc[4][4][4];
-    gemm_tile<true>(S, H, acc, sm, sm + 2 * kBM * kLds);
-
-    const float* tsp = shared ? P.sh_gu_tscale : P.gu_tscale + 2 * tr.slot;
-    const float tsg = __ldg(tsp), tsu = __ldg(tsp + 1);
-    uint16_t* out = shared ? P.hs : P.h;
-    const int lane = tid & 31, wn = (tid >> 5) & 3;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; q += 2) {
-            const int r = acc_row(i, q);
-            if (r >= tr.n_rows) continue;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int ii = i0 + wn * 16 + j * 8 + (lane & 3) * 2;
-                if (ii >= Ir) continue;
-                const float h0 = silu_f32(acc[i][j][q] * tsg) * (acc[i][j + 2][q] * tsu);
-                const float h1 = silu_f32(acc[i][j][q + 1] * tsg) * (acc[i][j + 2][q + 1] * tsu);
-                *reinterpret_cast<uint32_t*>(out + (size_t)(tr.p0 + r) * Ir + ii) = pack_bf16x2(h0, h1);
-            }
-        }
-}
-
-// 5. down GEMM: tile (mt, nt) = 128 rows of slot s x 128 output features. The
-//    epilogue scales by the routing weight and the tensor scale of D_e (or by
-//    sigmoid(gate) and the shared tensor scale) and writes row (t, j) of Y, where
-//    j is the entry's top-k slot (k for the shared expert).
-__global__ void __launch_bounds__(kGThreads, 2) grouped_down_kernel(const GroupedParams P, int n_tiles) {
-    __shared__ __align__(128) uint16_t sm[4 * kBM * kLds];
-    const int nt = blockIdx.x % n_tiles, mt = blockIdx.x / n_tiles;
-    TileRows tr;
-    if (!locate_tile(P, mt, &tr)) return;
-    const bool shared = tr.slot == P.E;
-    const int Kd = shared ? P.Is : P.I;
-    const int n0 = nt * kBN;
-    const int tid = threadIdx.x, H = P.H, k = P.k;
-
-    TileSrc S{};
-    S.dummy = P.x;
-    const uint16_t* hin = shared ? P.hs : P.h;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        const int r = (tid >> 2) + 64 * c;
-        if (r < tr.n_rows) S.a[c] = hin + (size_t)(tr.p0 + r) * Kd;
-    }
-    {
-        const int row = n0 + (tid >> 1);
-        if (row < H) {
-            const uint8_t* pk = shared ? P.sh_dn_packed : P.dn_packed + (size_t)tr.slot * H * (P.I / 2);
-            const uint8_t* sc = shared ? P.sh_dn_scales : P.dn_scales + (size_t)tr.slot * H * (P.I / 16);
-            S.bq = pk + (size_t)row * (Kd / 2);
-            S.bs = sc + (size_t)row * (Kd / 16);
-        }
-    }
-    float acc[4][4][4];
-    gemm_tile<true>(S, Kd, acc, sm, sm + 2 * kBM * kLds);
-
-    const float ts = __ldg(shared ? P.sh_dn_tscale : P.dn_tscale + tr.slot);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; q += 2) {
-            const int r = acc_row(i, q);
-            if (r >= tr.n_rows) continue;
-            int t, slot;
-            float sc;
-            if (shared) {
-                t = tr.p0 + r;
-                slot = k;
-                sc = sigmoid_f32(__ldg(P.gate + t)) * ts;
-            } else {
-                const int idx = __ldg(P.token_list + tr.p0 + r);
-                t = idx / k;
-                slot = idx - t * k;
-                sc = __ldg(P.w + idx) * ts;
-            }
-            float* yrow = P.Y + ((size_t)t * (k + 1) + slot) * H;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int col = n0 + acc_col(j, q);
-                if (col < H) *reinterpret_cast<float2*>(yrow + col) = make_float2(acc[i][j][q] * sc, acc[i][j][q + 1] * sc);
-            }
-        }
 }
 
 // 6. combine: y[t] = sum over the token's k routed rows, then the shared row, in
@@ -522,8 +349,11 @@ size_t align256p(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
+// The grouped tcgen05 GEMMs step K by 64 and copy 4-byte scale groups: H, I and Is
+// multiples of 64, E4M3 scales (their products with E2M1 values are exact in bf16).
 bool prefill_supported(const moe_layer_desc& d, int T) {
-    return T > NVFP4_DECODE_MAX_TOKENS && d.kind == NVFP4_SCALE_E4M3;
+    return T > NVFP4_DECODE_MAX_TOKENS && d.kind == NVFP4_SCALE_E4M3 && d.H % 64 == 0 && d.I % 64 == 0 &&
+           d.Is % 64 == 0;
 }
 
 size_t prefill_ws_bytes(const moe_layer_desc& d, int T) {
@@ -536,7 +366,7 @@ size_t prefill_ws_bytes(const moe_layer_desc& d, int T) {
     b += align256p(sizeof(float) * Tk);                         // w
     b += align256p(sizeof(int32_t) * nb * d.E);                 // bcount
     b += align256p(sizeof(int32_t) * (size_t)(d.E + 1));        // offsets
-    b += align256p(sizeof(int32_t) * (size_t)(d.E + 2));        // mt_prefix
+    b += align256p(sizeof(int32_t) * (size_t)(d.E + 2));        // tile_prefix
     b += align256p(sizeof(int32_t) * Tk);                       // token_list
     b += align256p(sizeof(uint16_t) * Tk * d.I);                // h
     b += align256p(sizeof(uint16_t) * (size_t)T * d.Is);        // hs
@@ -557,7 +387,7 @@ PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T) {
     w.w = reinterpret_cast<float*>(take(sizeof(float) * Tk));
     w.bcount = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * nb * d.E));
     w.offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(d.E + 1)));
-    w.mt_prefix = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(d.E + 2)));
+    w.tile_prefix = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(d.E + 2)));
     w.token_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * Tk));
     w.h = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * Tk * d.I));
     w.hs = reinterpret_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)T * d.Is));
@@ -569,7 +399,8 @@ PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T) {
 int prefill_launch_count(const moe_layer_desc& d) { return d.Is > 0 ? 9 : 8; }
 
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
-                               int32_t* ids_out, float* w_out, const PrefillWs& ws, cudaStream_t s) {
+                               int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
+                               cudaStream_t s) {
     const int E = d.E, k = d.k, H = d.H;
     const int total = T * k;
     int32_t* ids = ids_out ? ids_out : ws.ids;
@@ -593,7 +424,7 @@ cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T
     lists_hist_kernel<<<nb, kLB, 0, s>>>(ids, total, E, ws.bcount);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     lists_scan_kernel<<<1, NVFP4_MAX_EXPERTS, 0, s>>>(ws.bcount, nb, E, d.Is > 0 ? T : 0, ws.offsets,
-                                                       ws.mt_prefix);
+                                                       ws.tile_prefix);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     lists_place_kernel<<<nb, kLB, 0, s>>>(ids, total, E, ws.bcount, ws.token_list);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -606,25 +437,16 @@ cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T
     P.sh_gu_tscale = d.sh_gu_tscale;
     P.sh_dn_packed = d.sh_dn_packed; P.sh_dn_scales = static_cast<const uint8_t*>(d.sh_dn_scales);
     P.sh_dn_tscale = d.sh_dn_tscale;
-    P.offsets = ws.offsets; P.token_list = ws.token_list; P.mt_prefix = ws.mt_prefix;
+    P.offsets = ws.offsets; P.token_list = ws.token_list; P.tile_prefix = ws.tile_prefix;
     P.w = w; P.gate = ws.gate; P.h = ws.h; P.hs = ws.hs; P.Y = ws.Y;
-    // upper bound on the number of 128-row tiles: every non-empty expert adds at
-    // most one partial tile
+    // upper bound on the number of token tiles: every non-empty expert adds at most
+    // one partial tile
     const int nonempty = min(E, total);
-    const long long mt_max = ((long long)total + (long long)(kBM - 1) * nonempty) / kBM +
-                             (d.Is > 0 ? (T + kBM - 1) / kBM : 0);
-    // 4. gate/up + SwiGLU
-    {
-        const int nt = (max(d.I, d.Is) + 63) / 64;
-        grouped_gateup_kernel<<<(unsigned)(mt_max * nt), kGThreads, 0, s>>>(P, nt);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
-    // 5. down, scaled into Y
-    {
-        const int nt = (H + kBN - 1) / kBN;
-        grouped_down_kernel<<<(unsigned)(mt_max * nt), kGThreads, 0, s>>>(P, nt);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
+    const long long tiles_max = ((long long)total + (long long)(kTokTile - 1) * nonempty) / kTokTile +
+                                (d.Is > 0 ? (T + kTokTile - 1) / kTokTile : 0);
+    // 4. gate/up + SwiGLU, 5. down scaled into Y
+    if ((err = launch_grouped_tc(P, 0, (int)tiles_max, ws.hdr, wait_limit, s)) != cudaSuccess) return err;
+    if ((err = launch_grouped_tc(P, 1, (int)tiles_max, ws.hdr, wait_limit, s)) != cudaSuccess) return err;
     // 6. combine
     {
         const size_t n = (size_t)T * (H / 4);
