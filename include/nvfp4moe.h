@@ -214,7 +214,7 @@ NVFP4_API nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E,
  *   Paths: T == 1 runs the one-launch decode kernel (H % 256 == 0, H <= 2048,
  *   k*I + Is <= 8192; otherwise the multi-token path), 2 <= T <= 64 the
  *   multi-token decode kernels, T > 64 with E4M3 scales and H, I, Is multiples
- *   of 64 the grouped prefill path (tcgen05 tensor-core GEMMs with the weights
+ *   of 256 the grouped prefill path (tcgen05 tensor-core GEMMs with the weights
  *   expanded to bf16 in shared memory; the SwiGLU intermediate is rounded to
  *   bf16 there, the activation type). Other layers with T > 64 run as 64-token
  *   chunks of the multi-token path.

@@ -20,13 +20,17 @@
 // small experts waste no MMA work on padding and each weight tile is expanded once
 // for up to 256 tokens.
 //
-// Pipeline per CTA (288 threads): warps 0-7 stage the operands of K step kt + S - 1
-// with cp.async (token rows into the 128-byte-swizzled B tile, raw NVFP4 bytes into
-// a staging area), expand the NVFP4 bytes of step kt to bf16 in the swizzled A tile,
-// and arrive on full[kt % S]; warp 8 (one lane) waits on full, issues the MMAs and
-// commits them to empty[kt % S]; after the last step it commits to the accumulator
-// barrier, and warps 0-7 read TMEM, run the epilogue through shared memory and store
-// coalesced rows. Every wait is bounded; a wait that runs out records
+// Warp roles per CTA (416 threads), ring of S stages:
+//   warps 8-11 (loaders): for step s, wait until the MMAs of step s - S are done,
+//     cp.async the token rows into the 128-byte-swizzled B tile and the raw NVFP4
+//     bytes of the weight rows into a staging area, then let the copies themselves
+//     arrive on full_ld[s % S] (cp.async.mbarrier.arrive.noinc);
+//   warps 0-7 (expanders): wait on full_ld, expand the NVFP4 bytes into the
+//     swizzled bf16 A tile, fence to the async proxy, arrive on full_a;
+//   warp 12 (one lane): wait on full_ld and full_a, issue the MMAs, commit them to
+//     empty[s % S]; after the last step, commit to the accumulator barrier;
+//   warps 0-7 then read TMEM, run the epilogue through shared memory and store
+//     coalesced rows. Every wait is bounded; a wait that runs out records
 // NVFP4_ERR_DEVICE_TIMEOUT and makes every later wait of the CTA give up at once.
 //
 // NVFP4 -> bf16 expansion (exact): cvt.rn.f16x2.e2m1x2 gives the E2M1 values as
@@ -34,6 +38,12 @@
 // bf16 of the same value times 2^-112; one bf16x2 multiply by (block scale * 2^112)
 // restores the scale. Every product has at most 6 significant bits and lies in
 // [2^-10, 2688], so no step rounds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -43,25 +53,27 @@ namespace {
 
 constexpr int kM = 128;           // weight rows per accumulator (MMA M)
 constexpr int kKS = 64;           // K elements per stage: one 128-byte row of the swizzle atom
-constexpr int kProd = 256;        // operand / epilogue threads (warps 0-7)
-constexpr int kTcThreads = kProd + 32;
+constexpr int kRows = 2 * kM;     // weight rows per CTA: two accumulators share the token tile
+constexpr int kExp = 512;         // expander / epilogue threads (warps 0-15): half a weight row each
+constexpr int kLd = 128;          // operand loader threads (warps 16-19)
+constexpr int kMmaWarp = (kExp + kLd) / 32;   // warp 20: TMEM owner and MMA issuer
+constexpr int kTcThreads = kExp + kLd + 32;
+constexpr int kMaxStages = 8;
 
-template <int kParts>
-struct TcLayout {
-    static constexpr int kStages = kParts == 2 ? 3 : 4;
-    static constexpr int kA = kParts * kM * 128;               // A tile bytes per stage
-    static constexpr int kB = kTokTile * 128;                  // B tile bytes per stage
-    static constexpr int kStage = kA + kB;
-    static constexpr int kCodeT = kParts == 2 ? 32 : 16;       // raw code bytes per thread per stage
-    static constexpr int kRawCodes = kProd * kCodeT;
-    static constexpr int kRawStage = kRawCodes + kProd * 4;    // + 4 scale bytes per thread
-    static constexpr int kOffRaw = kStages * kStage;
-    static constexpr int kOffCols = kOffRaw + kStages * kRawStage;  // per token column: (Y row, scale)
-    static constexpr int kOffBar = kOffCols + kTokTile * 8;
-    static constexpr int kBytes = kOffBar + (2 * kStages + 1) * 8 + 16;
-    static constexpr int kTmemCols = kParts == 2 ? 512 : 256;
-    static constexpr int kAccStride = 256;                     // TMEM column offset of the up accumulator
-};
+// Dynamic shared memory: [1024-byte alignment slack][stage ring][fixed tables]. A
+// stage holds the bf16 A tile (kRows x 64, swizzled), the bf16 B tile (N x 64,
+// swizzled; N = the tile's token count rounded up to 16) and the raw NVFP4 bytes
+// of the A rows (TMA boxes); the number of stages follows from N.
+constexpr int kA = kRows * 128;
+constexpr int kRawScales = kRows * 32;      // raw: codes [kRows][32 B], then scales [kRows][16 B]
+constexpr int kRawStage = kRows * 48;       // (the 16 scale bytes hold 4 K steps; step s uses bytes 4(s%4)..)
+constexpr int kRing = 220 * 1024;
+constexpr int kOffTok = kRing;                          // per token row: source row (-1: none)
+constexpr int kOffCols = kOffTok + kTokTile * 4;        // per token column: (Y row, scale)
+constexpr int kOffBar = kOffCols + kTokTile * 8;
+constexpr int kSmemBytes = 1024 + kOffBar + (3 * kMaxStages + 1) * 8 + 16;
+constexpr int kTmemCols = 512;
+constexpr int kAccStride = 256;   // TMEM column offset of the second accumulator
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -69,12 +81,24 @@ __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvt
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+
+// Arrive on `bar` when every cp.async issued so far by this thread has landed (the
+// arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(su32(bar)) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// 2D tensor copy global -> shared (TMA), completing on `bar`'s transaction count.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)) : "memory");
+}
+
+// Bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
 
 // generic-proxy writes to shared memory -> visible to the tensor cores' async proxy
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -175,6 +199,19 @@ __device__ __forceinline__ void expand8(uint32_t w, uint32_t s2, uint32_t (&o)[4
     }
 }
 
+// ---------------------------------------------------------------- tensor maps
+// The grouped GEMMs read the NVFP4 weights through TMA: for each matrix group, the
+// codes as a 2D byte tensor [rows, K/2] (box 32 bytes x 128 rows = one K step of
+// 128 weight rows) and the block scales as [rows, K/16] (box 16 bytes x 128 rows =
+// four K steps); the down GEMM also reads its token rows h / hs as bf16 [rows, K]
+// with the 128-byte swizzle (box 64 x 16 rows).
+struct TcMaps {
+    CUtensorMap gu_codes, gu_scales, dn_codes, dn_scales;
+    CUtensorMap sh_gu_codes, sh_gu_scales, sh_dn_codes, sh_dn_scales;
+    CUtensorMap h, hs;
+};
+constexpr int kBoxRowsB = 16;   // token rows per B box of the down GEMM
+
 // ---------------------------------------------------------------- tiles
 struct TcTile {
     int slot;     // routed expert, or E for the shared expert
@@ -224,11 +261,12 @@ constexpr int kHS = kM + 8;   // bf16 staging row stride of the gate/up epilogue
 constexpr int kYS = kM + 4;   // fp32 staging row stride of the down epilogue
 
 // ---------------------------------------------------------------- kernel
-template <int kParts>
+// kMode 0: gate/up (A rows 0-127 = gate rows, 128-255 = the matching up rows of 128
+// intermediate indices), kMode 1: down (A rows = 256 consecutive output features).
+template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
-grouped_tc_kernel(const GroupedParams P, int n_ft, WsHeader* hdr, unsigned long long wait_limit) {
-    using L = TcLayout<kParts>;
-    constexpr int S = L::kStages;
+grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, int n_ft, WsHeader* hdr,
+                  unsigned long long wait_limit) {
     extern __shared__ uint8_t tc_smem_raw[];
     // the swizzle pattern follows shared-memory address bits: align the base to 1024
     uint8_t* sm = tc_smem_raw + ((1024u - (su32(tc_smem_raw) & 1023u)) & 1023u);
@@ -237,25 +275,30 @@ grouped_tc_kernel(const GroupedParams P, int n_ft, WsHeader* hdr, unsigned long 
     TcTile tr;
     if (!locate_tc_tile(P, tt, &tr)) return;
     const bool shared = tr.slot == P.E;
-    const int Fvalid = kParts == 2 ? (shared ? P.Is : P.I) : P.H;   // output features of this GEMM
-    const int feat0 = ft * kM;
+    const int Fvalid = kMode == 0 ? (shared ? P.Is : P.I) : P.H;   // output features of this GEMM
+    const int feat0 = ft * (kMode == 0 ? kM : kRows);
     if (feat0 >= Fvalid) return;
-    const int Kd = kParts == 2 ? P.H : (shared ? P.Is : P.I);
+    const int Kd = kMode == 0 ? P.H : (shared ? P.Is : P.I);
     const int nk = Kd / kKS;
     const int N = (tr.n_rows + 15) & ~15;
+    const int stage_bytes = kA + N * 128 + kRawStage;   // multiple of 1024
+    const int S = min(kMaxStages, kRing / stage_bytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::kOffBar);
-    uint64_t* empty = full + S;
-    uint64_t* accb = empty + S;
+    uint64_t* full_ld = reinterpret_cast<uint64_t*>(sm + kOffBar);   // B rows and raw weights landed
+    uint64_t* full_a = full_ld + kMaxStages;                          // A tile expanded
+    uint64_t* empty = full_a + kMaxStages;                            // MMAs of the stage done
+    uint64_t* accb = empty + kMaxStages;                              // all MMAs done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int2* cols = reinterpret_cast<int2*>(sm + L::kOffCols);
+    int* tok = reinterpret_cast<int*>(sm + kOffTok);
+    int2* cols = reinterpret_cast<int2*>(sm + kOffCols);
 
-    if (warp == kProd / 32) {
+    if (warp == kMmaWarp) {
         if (lane == 0) {
             for (int i = 0; i < S; ++i) {
-                mbar_init(&full[i], kProd);
+                mbar_init(&full_ld[i], kMode == 0 ? kLd + 1 : 1);
+                mbar_init(&full_a[i], kExp);
                 mbar_init(&empty[i], 1);
             }
             mbar_init(accb, 1);
@@ -263,11 +306,18 @@ grouped_tc_kernel(const GroupedParams P, int n_ft, WsHeader* hdr, unsigned long 
             fence_mbar_init();
         }
         __syncwarp();
-        tmem_alloc<L::kTmemCols>(tmem_slot);
+        tmem_alloc<kTmemCols>(tmem_slot);
     }
-    if (kParts == 1) {
-        // per token column of the tile: its row of Y and the epilogue scale
-        for (int c = tid; c < tr.n_rows; c += kTcThreads) {
+    // per token row: the row of x (gate/up) or of h / hs (down) it reads; -1 past the tile
+    for (int c = tid; c < kTokTile; c += kTcThreads) {
+        int src = -1;
+        if (c < tr.n_rows) {
+            if (kMode == 0 && !shared) src = __ldg(P.token_list + tr.p0 + c) / P.k;
+            else src = tr.p0 + c;
+        }
+        tok[c] = src;
+        if (kMode == 1 && c < tr.n_rows) {
+            // the row of Y this column feeds and the epilogue scale
             int t, j;
             float sc;
             if (shared) {
@@ -289,220 +339,300 @@ grouped_tc_kernel(const GroupedParams P, int n_ft, WsHeader* hdr, unsigned long 
     const uint32_t tmem = *tmem_slot;
     const uint32_t sm_base = su32(sm);
 
-    if (warp < kProd / 32) {
-        // ---------------- operand producers
-        const uint8_t* a_codes = nullptr;   // this thread's weight bytes at K step 0
-        const uint8_t* a_scales = nullptr;
-        if (kParts == 2) {
-            const int part = tid >> 7, f = feat0 + (tid & 127);
-            if (f < Fvalid) {
-                const size_t wrow = (size_t)(part == 0 ? f : Fvalid + f);   // gate rows, then up rows
-                const uint8_t* pk = shared ? P.sh_gu_packed : P.gu_packed + (size_t)tr.slot * 2 * P.I * (P.H / 2);
-                const uint8_t* sc = shared ? P.sh_gu_scales : P.gu_scales + (size_t)tr.slot * 2 * P.I * (P.H / 16);
-                a_codes = pk + wrow * (P.H / 2);
-                a_scales = sc + wrow * (P.H / 16);
-            }
+    // weight row r (0 .. kRows-1) of the tile: its packed codes and E4M3 scales
+    auto weight_row = [&](int r, const uint8_t** codes, const uint8_t** scales) {
+        *codes = nullptr;
+        *scales = nullptr;
+        if (kMode == 0) {
+            const int f = feat0 + (r & (kM - 1));
+            if (f >= Fvalid) return;
+            const size_t wrow = (size_t)(r < kM ? f : Fvalid + f);   // gate rows, then up rows
+            const uint8_t* pk = shared ? P.sh_gu_packed : P.gu_packed + (size_t)tr.slot * 2 * P.I * (P.H / 2);
+            const uint8_t* sc = shared ? P.sh_gu_scales : P.gu_scales + (size_t)tr.slot * 2 * P.I * (P.H / 16);
+            *codes = pk + wrow * (P.H / 2);
+            *scales = sc + wrow * (P.H / 16);
         } else {
-            const int f = feat0 + (tid >> 1);
-            if (f < P.H) {
-                const uint8_t* pk = shared ? P.sh_dn_packed : P.dn_packed + (size_t)tr.slot * P.H * (P.I / 2);
-                const uint8_t* sc = shared ? P.sh_dn_scales : P.dn_scales + (size_t)tr.slot * P.H * (P.I / 16);
-                a_codes = pk + (size_t)f * (Kd / 2) + (tid & 1) * 16;
-                a_scales = sc + (size_t)f * (Kd / 16);
-            }
+            const int f = feat0 + r;
+            if (f >= P.H) return;
+            const uint8_t* pk = shared ? P.sh_dn_packed : P.dn_packed + (size_t)tr.slot * P.H * (P.I / 2);
+            const uint8_t* sc = shared ? P.sh_dn_scales : P.dn_scales + (size_t)tr.slot * P.H * (P.I / 16);
+            *codes = pk + (size_t)f * (Kd / 2);
+            *scales = sc + (size_t)f * (Kd / 16);
         }
-        // token rows: 16-byte chunk (tid & 7) of rows (tid >> 3) + 32 j
-        const uint16_t* brow[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int row = (tid >> 3) + 32 * j;
-            brow[j] = nullptr;
-            if (row < tr.n_rows) {
-                if (kParts == 2) {
-                    const int tok = shared ? tr.p0 + row : __ldg(P.token_list + tr.p0 + row) / P.k;
-                    brow[j] = P.x + (size_t)tok * P.H;
-                } else {
-                    brow[j] = (shared ? P.hs : P.h) + (size_t)(tr.p0 + row) * Kd;
-                }
-            }
+    };
+
+    if (warp >= kExp / 32 && warp < kMmaWarp) {
+        // ---------------- loaders: weight codes and scales (TMA, one thread), token rows
+        // (gate/up: gathered rows of x by cp.async from all loader threads; down: the
+        // tile's contiguous rows of h / hs by TMA)
+        const int lt = tid - kExp;
+        const CUtensorMap* mc = kMode == 0 ? (shared ? &maps.sh_gu_codes : &maps.gu_codes)
+                                           : (shared ? &maps.sh_dn_codes : &maps.dn_codes);
+        const CUtensorMap* ms = kMode == 0 ? (shared ? &maps.sh_gu_scales : &maps.gu_scales)
+                                           : (shared ? &maps.sh_dn_scales : &maps.dn_scales);
+        int y0, y1;   // first weight row of A rows 0-127 and 128-255
+        if (kMode == 0) {
+            const int base = shared ? 0 : tr.slot * 2 * P.I;
+            y0 = base + feat0;
+            y1 = base + Fvalid + feat0;
+        } else {
+            y0 = (shared ? 0 : tr.slot * P.H) + feat0;
+            y1 = y0 + kM;
         }
-        const int bc = tid & 7;
-
-        auto issue = [&](int s) {
-            const int st = s % S;
-            const uint32_t bt = sm_base + st * L::kStage + L::kA;
+        const uint32_t tx = 2 * (32 * kM) + 2 * (16 * kM) + (kMode == 1 ? N * 128 : 0);
+        const uint16_t* bsrc = P.x;
+        const int bc = lt & 7;
+        int boff[16];   // gate/up: element offset of this thread's chunk in row (lt >> 3) + 16 j, or -1
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int row = (tid >> 3) + 32 * j;
-                if (row < N) {
-                    const uint32_t dst = bt + row * 128 + ((bc ^ (row & 7)) << 4);
-                    if (brow[j]) cp_async16_zfill(dst, brow[j] + s * kKS + bc * 8, 16u);
-                    else cp_async16_zfill(dst, P.x, 0u);
-                }
-            }
-            if (a_codes) {
-                const uint32_t raw = sm_base + L::kOffRaw + st * L::kRawStage;
-                const uint32_t cd = raw + tid * L::kCodeT;
-                cp_async16_zfill(cd, a_codes + s * 32, 16u);
-                if (kParts == 2) cp_async16_zfill(cd + 16, a_codes + s * 32 + 16, 16u);
-                cp_async4(raw + L::kRawCodes + tid * 4, a_scales + s * 4);
-            }
-            cp_async_commit_group();
-        };
-
-        auto expand = [&](int kt) {
-            const int st = kt % S;
-            uint8_t* stage = sm + st * L::kStage;
-            const uint8_t* raw = sm + L::kOffRaw + st * L::kRawStage;
-            if (kParts == 2) {
-                const int r = tid & 127;
-                uint8_t* arow = stage + (tid >> 7) * (kM * 128) + r * 128;
-                if (a_codes) {
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(raw + tid * 32);
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(raw + tid * 32 + 16);
-                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(raw + L::kRawCodes + tid * 4);
-                    uint32_t sc[4];
-                    scale_pair_bf16(sw, sc[0], sc[1]);
-                    scale_pair_bf16(sw >> 16, sc[2], sc[3]);
-                    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {   // chunk c = elements 8c..8c+7 of the step, block c/2
-                        uint32_t o[4];
-                        expand8(words[c], sc[c >> 1], o);
-                        *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(arow + (c << 4)) = make_uint4(0, 0, 0, 0);
-                }
+        for (int j = 0; j < 16; ++j) {
+            const int src = tok[(lt >> 3) + 16 * j];
+            boff[j] = src < 0 ? -1 : src * P.H + bc * 8;
+        }
+        if (lt == 0) {
+            // the CTA reads its weight rows once, over the whole K loop: start them all
+            // towards L2 now
+            if (kMode == 0) {
+                const int rows = min(kM, Fvalid - feat0);
+                const uint8_t* pk = shared ? P.sh_gu_packed : P.gu_packed;
+                const uint8_t* sc = shared ? P.sh_gu_scales : P.gu_scales;
+                bulk_prefetch_l2(pk + (size_t)y0 * (P.H / 2), (uint32_t)rows * (P.H / 2));
+                bulk_prefetch_l2(pk + (size_t)y1 * (P.H / 2), (uint32_t)rows * (P.H / 2));
+                bulk_prefetch_l2(sc + (size_t)y0 * (P.H / 16), (uint32_t)rows * (P.H / 16));
+                bulk_prefetch_l2(sc + (size_t)y1 * (P.H / 16), (uint32_t)rows * (P.H / 16));
             } else {
-                const int r = tid >> 1, half = tid & 1;
-                uint8_t* arow = stage + r * 128;
-                if (a_codes) {
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(raw + tid * 16);
-                    const uint32_t sw = *reinterpret_cast<const uint32_t*>(raw + L::kRawCodes + tid * 4);
-                    uint32_t s0, s1;
-                    scale_pair_bf16(sw >> (16 * half), s0, s1);
-                    const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {   // chunk 4 half + c, block 2 half + c/2
-                        uint32_t o[4];
-                        expand8(words[c], c < 2 ? s0 : s1, o);
-                        const int ch = 4 * half + c;
-                        *reinterpret_cast<uint4*>(arow + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(arow + ((4 * half + c) << 4)) = make_uint4(0, 0, 0, 0);
-                }
+                const int rows = min(kRows, P.H - feat0);
+                const uint8_t* pk = shared ? P.sh_dn_packed : P.dn_packed;
+                const uint8_t* sc = shared ? P.sh_dn_scales : P.dn_scales;
+                bulk_prefetch_l2(pk + (size_t)y0 * (Kd / 2), (uint32_t)rows * (Kd / 2));
+                bulk_prefetch_l2(sc + (size_t)y0 * (Kd / 16), (uint32_t)rows * (Kd / 16));
             }
-        };
-
-#pragma unroll 1
-        for (int s = 0; s < S - 1; ++s) {
-            if (s < nk) issue(s);
-            else cp_async_commit_group();
         }
+        if (kMode == 0 || lt == 0) {
+            int st = 0, use = 0;   // ring slot of step s and how many times it was filled before
+#pragma unroll 1
+            for (int s = 0; s < nk; ++s) {
+                if (use > 0) wait_or_abort(&empty[st], (use - 1) & 1, abort_flag, hdr, wait_limit);
+                const uint32_t stage = sm_base + st * stage_bytes;
+                const uint32_t bt = stage + kA;
+                const uint32_t raw = bt + N * 128;
+                if (lt == 0) {
+                    mbar_arrive_expect_tx(&full_ld[st], tx);
+                    tma_load_2d(raw, mc, s * 32, y0, &full_ld[st]);
+                    tma_load_2d(raw + kM * 32, mc, s * 32, y1, &full_ld[st]);
+                    tma_load_2d(raw + kRawScales, ms, (s >> 2) * 16, y0, &full_ld[st]);
+                    tma_load_2d(raw + kRawScales + kM * 16, ms, (s >> 2) * 16, y1, &full_ld[st]);
+                    if (kMode == 1) {
+                        const CUtensorMap* mb = shared ? &maps.hs : &maps.h;
+                        for (int i = 0; i < N / kBoxRowsB; ++i)
+                            tma_load_2d(bt + i * (kBoxRowsB * 128), mb, s * kKS, tr.p0 + i * kBoxRowsB, &full_ld[st]);
+                    }
+                }
+                if (kMode == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int row = (lt >> 3) + 16 * j;
+                        if (row < N) {
+                            const uint32_t dst = bt + row * 128 + ((bc ^ (row & 7)) << 4);
+                            if (boff[j] >= 0) cp_async16_zfill(dst, bsrc + boff[j] + s * kKS, 16u);
+                            else cp_async16_zfill(dst, P.x, 0u);
+                        }
+                    }
+                    cp_async_arrive_noinc(&full_ld[st]);
+                }
+                if (++st == S) { st = 0; ++use; }
+            }
+        }
+    } else if (warp < kExp / 32) {
+        // ---------------- expanders: raw NVFP4 bytes -> bf16 A tile (half a row each)
+        const uint8_t* rcode;
+        const uint8_t* rscale;
+        const int r = tid >> 1, half = tid & 1;
+        weight_row(r, &rcode, &rscale);
+        const bool valid = rcode != nullptr;
+        const int rl = r & 7;   // swizzle phase of the row
+        const int a_off = (r >> 7) * (kM * 128) + (r & (kM - 1)) * 128;
+        int st = 0, ph = 0;
 #pragma unroll 1
         for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt + S - 1;
-            if (s < nk) {
-                if (s >= S) wait_or_abort(&empty[s % S], ((s / S) - 1) & 1, abort_flag, hdr, wait_limit);
-                issue(s);
+            wait_or_abort(&full_ld[st], ph, abort_flag, hdr, wait_limit);
+            uint8_t* stage = sm + st * stage_bytes;
+            uint8_t* arow = stage + a_off;
+            const uint8_t* raw = stage + kA + N * 128;
+            if (valid) {
+                const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 32 + half * 16);
+                const uint32_t sw = *reinterpret_cast<const uint32_t*>(raw + kRawScales + r * 16 + (kt & 3) * 4);
+                uint32_t s0, s1;
+                scale_pair_bf16(sw >> (16 * half), s0, s1);
+                const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {   // chunk 4 half + c = elements 8(4 half + c) .., block 2 half + c/2
+                    uint32_t o[4];
+                    expand8(words[c], c < 2 ? s0 : s1, o);
+                    *reinterpret_cast<uint4*>(arow + (((4 * half + c) ^ rl) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
             } else {
-                cp_async_commit_group();
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(arow + ((4 * half + c) << 4)) = make_uint4(0, 0, 0, 0);
             }
-            cp_async_wait_group<S - 1>();
-            expand(kt);
             fence_proxy_async_smem();
-            mbar_arrive(&full[kt % S]);
+            mbar_arrive(&full_a[st]);
+            if (++st == S) { st = 0; ph ^= 1; }
         }
 
         // ---------------- epilogue: TMEM -> registers -> shared staging -> global
         wait_or_abort(accb, 0, abort_flag, hdr, wait_limit);
         tc_fence_after();
-        const int q = warp & 3, c_begin = (warp >> 2) * (kTokTile / 2);
+        const int q = warp & 3, c_begin = (warp >> 2) * (kTokTile / 4);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const int f = 32 * q + lane;
-        if (kParts == 2) {
+        if (kMode == 0) {
             uint16_t* stg = reinterpret_cast<uint16_t*>(sm);
             const float* tsp = shared ? P.sh_gu_tscale : P.gu_tscale + 2 * tr.slot;
             const float tsg = __ldg(tsp), tsu = __ldg(tsp + 1);
 #pragma unroll 1
-            for (int c0 = c_begin; c0 < c_begin + kTokTile / 2 && c0 < N; c0 += 16) {
+            for (int c0 = c_begin; c0 < c_begin + kTokTile / 4 && c0 < N; c0 += 16) {
                 float g[16], u[16];
                 tmem_ld16(lane_base + c0, g);
-                tmem_ld16(lane_base + L::kAccStride + c0, u);
+                tmem_ld16(lane_base + kAccStride + c0, u);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     stg[(c0 + j) * kHS + f] = f32_to_bf16(silu_f32(g[j] * tsg) * (u[j] * tsu));
             }
-        } else {
-            float* stg = reinterpret_cast<float*>(sm);
-#pragma unroll 1
-            for (int c0 = c_begin; c0 < c_begin + kTokTile / 2 && c0 < N; c0 += 16) {
-                float a[16];
-                tmem_ld16(lane_base + c0, a);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) stg[(c0 + j) * kYS + f] = a[j];
-            }
-        }
-        tc_fence_before();
-        named_bar_sync(1, kProd);
-        if (kParts == 2) {
-            const uint16_t* stg = reinterpret_cast<const uint16_t*>(sm);
+            tc_fence_before();
+            named_bar_sync(1, kExp);
             uint16_t* out = shared ? P.hs : P.h;
             const int ch = tid & 15;
             if (feat0 + 8 * ch < Fvalid) {
 #pragma unroll 4
-                for (int c = tid >> 4; c < tr.n_rows; c += kProd / 16)
+                for (int c = tid >> 4; c < tr.n_rows; c += kExp / 16)
                     *reinterpret_cast<uint4*>(out + (size_t)(tr.p0 + c) * Fvalid + feat0 + 8 * ch) =
                         *reinterpret_cast<const uint4*>(stg + c * kHS + 8 * ch);
             }
         } else {
-            const float* stg = reinterpret_cast<const float*>(sm);
-            const int ch = tid & 31;
-            if (feat0 + 4 * ch < P.H) {
-#pragma unroll 4
-                for (int c = tid >> 5; c < tr.n_rows; c += kProd / 32) {
-                    const int2 ci = cols[c];
-                    const float sc = __int_as_float(ci.y);
-                    float4 v = *reinterpret_cast<const float4*>(stg + c * kYS + 4 * ch);
-                    v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
-                    *reinterpret_cast<float4*>(P.Y + (size_t)ci.x * P.H + feat0 + 4 * ch) = v;
+            float* stg = reinterpret_cast<float*>(sm);
+#pragma unroll 1
+            for (int p = 0; p < 2; ++p) {
+                const int fp0 = feat0 + p * kM;
+                if (fp0 >= P.H) break;
+#pragma unroll 1
+                for (int c0 = c_begin; c0 < c_begin + kTokTile / 4 && c0 < N; c0 += 16) {
+                    float a[16];
+                    tmem_ld16(lane_base + p * kAccStride + c0, a);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[(c0 + j) * kYS + f] = a[j];
                 }
+                named_bar_sync(1, kExp);
+                const int ch = tid & 31;
+                if (fp0 + 4 * ch < P.H) {
+#pragma unroll 4
+                    for (int c = tid >> 5; c < tr.n_rows; c += kExp / 32) {
+                        const int2 ci = cols[c];
+                        const float sc = __int_as_float(ci.y);
+                        float4 v = *reinterpret_cast<const float4*>(stg + c * kYS + 4 * ch);
+                        v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
+                        *reinterpret_cast<float4*>(P.Y + (size_t)ci.x * P.H + fp0 + 4 * ch) = v;
+                    }
+                }
+                named_bar_sync(1, kExp);   // staging is reused by the next part
             }
+            tc_fence_before();
         }
     } else if (lane == 0) {
         // ---------------- MMA issuer (one thread)
         const uint32_t idesc = f16_idesc(kM, N);
+        int st = 0, ph = 0;
 #pragma unroll 1
         for (int kt = 0; kt < nk; ++kt) {
-            const int st = kt % S;
-            if (!wait_or_abort(&full[st], (kt / S) & 1, abort_flag, hdr, wait_limit)) break;
+            if (!wait_or_abort(&full_ld[st], ph, abort_flag, hdr, wait_limit)) break;
+            if (!wait_or_abort(&full_a[st], ph, abort_flag, hdr, wait_limit)) break;
+            // the B rows were written by cp.async (generic proxy): order them before the
+            // tensor cores' reads
+            fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t stage = sm_base + st * L::kStage;
+            const uint32_t stage = sm_base + st * stage_bytes;
 #pragma unroll
             for (int j = 0; j < kKS / 16; ++j) {
-                const uint64_t bd = sw128_desc(stage + L::kA + j * 32);
+                const uint64_t bd = sw128_desc(stage + kA + j * 32);
 #pragma unroll
-                for (int p = 0; p < kParts; ++p)
-                    tc_mma(tmem + p * L::kAccStride, sw128_desc(stage + p * (kM * 128) + j * 32), bd, idesc,
+                for (int p = 0; p < 2; ++p)
+                    tc_mma(tmem + p * kAccStride, sw128_desc(stage + p * (kM * 128) + j * 32), bd, idesc,
                            (kt | j) != 0);
             }
             tc_commit(&empty[st]);
+            if (++st == S) { st = 0; ph ^= 1; }
         }
         tc_commit(accb);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kProd / 32) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc<L::kTmemCols>(tmem);
+        tmem_dealloc<kTmemCols>(tmem);
     }
+}
+
+}  // namespace
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Byte matrix [rows, inner] read in boxes of box_inner bytes x 128 rows.
+bool encode_u8(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, uint64_t inner,
+               uint64_t rows, uint32_t box_inner) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner};
+    const cuuint32_t box[2] = {box_inner, (cuuint32_t)kM};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 matrix [rows, cols] read in boxes of 64 x kBoxRowsB, 128-byte swizzled in shared memory.
+bool encode_bf16_sw128(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, uint64_t cols,
+                       uint64_t rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kKS, (cuuint32_t)kBoxRowsB};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_maps(const GroupedParams& P, TcMaps* m) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn) return false;
+    memset(m, 0, sizeof(*m));
+    const uint64_t E = (uint64_t)P.E, H = (uint64_t)P.H, I = (uint64_t)P.I, Is = (uint64_t)P.Is;
+    bool ok = encode_u8(fn, &m->gu_codes, P.gu_packed, H / 2, E * 2 * I, 32) &&
+              encode_u8(fn, &m->gu_scales, P.gu_scales, H / 16, E * 2 * I, 16) &&
+              encode_u8(fn, &m->dn_codes, P.dn_packed, I / 2, E * H, 32) &&
+              encode_u8(fn, &m->dn_scales, P.dn_scales, I / 16, E * H, 16) &&
+              encode_bf16_sw128(fn, &m->h, P.h, I, (uint64_t)P.T * P.k);
+    if (ok && Is > 0)
+        ok = encode_u8(fn, &m->sh_gu_codes, P.sh_gu_packed, H / 2, 2 * Is, 32) &&
+             encode_u8(fn, &m->sh_gu_scales, P.sh_gu_scales, H / 16, 2 * Is, 16) &&
+             encode_u8(fn, &m->sh_dn_codes, P.sh_dn_packed, Is / 2, H, 32) &&
+             encode_u8(fn, &m->sh_dn_scales, P.sh_dn_scales, Is / 16, H, 16) &&
+             encode_bf16_sw128(fn, &m->hs, P.hs, Is, (uint64_t)P.T);
+    return ok;
 }
 
 }  // namespace
@@ -510,28 +640,23 @@ grouped_tc_kernel(const GroupedParams P, int n_ft, WsHeader* hdr, unsigned long 
 cudaError_t launch_grouped_tc(const GroupedParams& P, int mode, int tiles_max, WsHeader* hdr,
                               uint64_t wait_limit, cudaStream_t s) {
     if (tiles_max <= 0) return cudaSuccess;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[mode]) {
+        cudaError_t e = cudaFuncSetAttribute(mode == 0 ? grouped_tc_kernel<0> : grouped_tc_kernel<1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[mode] = true;
+    }
+    TcMaps maps;
+    if (!encode_maps(P, &maps)) return cudaErrorInvalidValue;
     if (mode == 0) {
-        using L = TcLayout<2>;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 L::kBytes + 1024);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
         const int n_ft = (max(P.I, P.Is) + kM - 1) / kM;
-        grouped_tc_kernel<2><<<(unsigned)tiles_max * n_ft, kTcThreads, L::kBytes + 1024, s>>>(P, n_ft, hdr, wait_limit);
+        grouped_tc_kernel<0><<<(unsigned)tiles_max * n_ft, kTcThreads, kSmemBytes, s>>>(P, maps, n_ft, hdr,
+                                                                                       wait_limit);
     } else {
-        using L = TcLayout<1>;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 L::kBytes + 1024);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
-        const int n_ft = (P.H + kM - 1) / kM;
-        grouped_tc_kernel<1><<<(unsigned)tiles_max * n_ft, kTcThreads, L::kBytes + 1024, s>>>(P, n_ft, hdr, wait_limit);
+        const int n_ft = (P.H + kRows - 1) / kRows;
+        grouped_tc_kernel<1><<<(unsigned)tiles_max * n_ft, kTcThreads, kSmemBytes, s>>>(P, maps, n_ft, hdr,
+                                                                                       wait_limit);
     }
     return cudaGetLastError();
 }

@@ -349,11 +349,12 @@ size_t align256p(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
-// The grouped tcgen05 GEMMs step K by 64 and copy 4-byte scale groups: H, I and Is
-// multiples of 64, E4M3 scales (their products with E2M1 values are exact in bf16).
+// The grouped tcgen05 GEMMs read the weights through TMA tensor maps whose row
+// strides (K/16 bytes for the scales) must be multiples of 16: H, I and Is
+// multiples of 256, E4M3 scales (their products with E2M1 values are exact in bf16).
 bool prefill_supported(const moe_layer_desc& d, int T) {
-    return T > NVFP4_DECODE_MAX_TOKENS && d.kind == NVFP4_SCALE_E4M3 && d.H % 64 == 0 && d.I % 64 == 0 &&
-           d.Is % 64 == 0;
+    return T > NVFP4_DECODE_MAX_TOKENS && d.kind == NVFP4_SCALE_E4M3 && d.H % 256 == 0 && d.I % 256 == 0 &&
+           d.Is % 256 == 0;
 }
 
 size_t prefill_ws_bytes(const moe_layer_desc& d, int T) {

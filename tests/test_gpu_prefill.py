@@ -55,33 +55,46 @@ def _sampled_parity(L, x, y, ids, w, rows, kind=0):
     return check_layer_parity(L, x[idx], y.cpu()[idx], ids.cpu()[idx], w.cpu()[idx], kind=kind)
 
 
+SM = wl.SMALL256
+
+
 @pytest.mark.parametrize("T", [65, 200, 777])
-def test_tiny_prefill(nv, T):
-    """Every token of a small layer: several 128-row tiles per expert and ragged tails."""
-    L = wl.LayerInputs(wl.TINY, seed=100 + T)
+def test_small_prefill(nv, T):
+    """Every token of a small layer on the grouped tensor-core path: several token
+    tiles per expert and ragged tails."""
+    L = wl.LayerInputs(SM, seed=100 + T)
     layer = gpu_layer(L)
-    x = wl.activations(100 + T, T, wl.TINY.H)
+    x = wl.activations(100 + T, T, SM.H)
     y, ids, w = _forward(nv, layer, x)
     check_layer_parity(L, x, y, ids, w)
 
 
-def test_tiny_prefill_no_shared_expert(nv):
-    L = wl.LayerInputs(wl.TINY, seed=7)
+def test_small_prefill_no_shared_expert(nv):
+    L = wl.LayerInputs(SM, seed=7)
     layer = gpu_layer(L, with_shared=False)
-    x = wl.activations(7, 300, wl.TINY.H)
+    x = wl.activations(7, 300, SM.H)
     y, ids, w = _forward(nv, layer, x)
     check_layer_parity(L, x, y, ids, w, with_shared=False)
 
 
-def test_tiny_prefill_skewed_routing(nv):
-    """Strongly skewed router: some experts get no tokens, others several tiles."""
-    shape = replace(wl.TINY, router_kappa=1.5)
+def test_small_prefill_skewed_routing(nv):
+    """Strongly skewed router: some experts get no tokens, others several 256-row tiles."""
+    shape = replace(SM, router_kappa=1.5)
     L = wl.LayerInputs(shape, seed=11)
     layer = gpu_layer(L)
-    x = wl.activations(11, 1000, shape.H)
+    x = wl.activations(11, 1600, shape.H)
     y, ids, w = _forward(nv, layer, x)
     counts = np.bincount(ids.cpu().numpy().ravel(), minlength=shape.E)
-    assert counts.max() > 256
+    assert counts.max() > 512
+    check_layer_parity(L, x, y, ids, w)
+
+
+def test_tiny_prefill_chunked(nv):
+    """I = 128 is outside the grouped path's shapes: 64-token chunks of the decode path."""
+    L = wl.LayerInputs(wl.TINY, seed=13)
+    layer = gpu_layer(L)
+    x = wl.activations(13, 150, wl.TINY.H)
+    y, ids, w = _forward(nv, layer, x)
     check_layer_parity(L, x, y, ids, w)
 
 
@@ -95,9 +108,9 @@ def test_tiny_prefill_fp16_scales(nv):
 
 
 def test_prefill_deterministic(nv):
-    L = wl.LayerInputs(wl.TINY, seed=3)
+    L = wl.LayerInputs(SM, seed=3)
     layer = gpu_layer(L)
-    x = wl.activations(3, 500, wl.TINY.H).cuda()
+    x = wl.activations(3, 500, SM.H).cuda()
     y1 = nv.moe_layer_forward(layer, x)
     y2 = nv.moe_layer_forward(layer, x)
     torch.cuda.synchronize()

@@ -137,6 +137,8 @@ class MoEShape:
 
 
 TINY = MoEShape(H=256, E=16, k=2, I=128, Is=128)
+# smallest shape whose prefill runs the grouped tensor-core path (H, I, Is multiples of 256)
+SMALL256 = MoEShape(H=256, E=16, k=2, I=256, Is=256)
 QWEN36_35B_A3B = MoEShape(H=2048, E=256, k=8, I=512, Is=512)
 
 
