@@ -39,6 +39,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seeds", type=int, default=N_SEEDS, help="layer instances to rotate over")
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"],
+                    help="decode: the single-token layer (default, the headline); prefill: one "
+                         "4096-token layer call with the skewed router")
     return ap.parse_args()
 
 
@@ -206,6 +209,99 @@ def step_bytes(layer, ids_row, T=1):
     return distinct * per_expert + shared + router + acts
 
 
+PREFILL_GOLDEN = os.path.join(ROOT, "tests", "golden", "prefill_zipf.json")
+
+
+def prefill_flops(shape, T, has_shared=True):
+    """Algorithmic FLOPs of one layer call: router GEMM, routed and shared SwiGLU experts."""
+    f = 2 * T * shape.E * shape.H + 2 * T * shape.k * 3 * shape.I * shape.H
+    if has_shared:
+        f += 2 * T * 3 * shape.Is * shape.H + 2 * T * shape.H
+    return f
+
+
+def run_prefill(args, nv, wl, device):
+    """One 4096-token call of the Qwen3.6-35B-A3B-shaped layer per step, router rows
+    scaled by rank^-kappa (kappa from the committed calibration) so that per-expert
+    token counts range from about 20 to 1000."""
+    import dataclasses
+    gold = json.load(open(PREFILL_GOLDEN))
+    shape = dataclasses.replace(wl.QWEN36_35B_A3B, router_kappa=gold["kappa"])
+    T, seed = gold["T"], gold["seed"]
+    L = wl.LayerInputs(shape, seed=seed)
+    layer = nv.MoELayer.allocate(shape.H, shape.E, shape.k, shape.I, shape.Is, nv.SCALE_E4M3, device)
+    layer.router_w.copy_(L.router_w(device))
+    for e in range(shape.E):
+        layer.pack_expert(e, *L.expert_f32(e, device=device))
+    layer.pack_shared(*L.shared_f32(device=device), L.shared_sigmoid_w(device))
+    x = wl.activations(seed, T, shape.H, device=device)
+    d = layer.desc()
+    ws = nv.Workspace(nv.moe_layer_workspace_size(layer, T), device=device)
+    y = torch.empty(T, shape.H, dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        nv.moe_layer_forward(layer, x, ws=ws, y=y, desc=d)
+    torch.cuda.synchronize()
+    K = max(1, args.steps)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index or 0) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(K):
+            nv.moe_layer_forward(layer, x, ws=ws, y=y, desc=d)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    ms = ev0.elapsed_time(ev1) / K
+    # end to end: pinned host x in, y out, every step
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+    xd = torch.empty_like(x)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    Ke = min(K, 20)
+    e0.record(stream)
+    for _ in range(Ke):
+        xd.copy_(xh, non_blocking=True)
+        nv.moe_layer_forward(layer, xd, ws=ws, y=y, desc=d)
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    flops = prefill_flops(shape, T)
+    tflops = flops / (ms * 1e-3) / 1e12
+    mp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak, kind = (json.load(open(mp)).get("bf16_tflops_sustained"), "measured (sustained)") if os.path.exists(mp) \
+        else (1700.0, "fallback (sustained)")
+    line = {
+        "metric": "NVFP4 MoE-layer prefill: us per 4096-token layer call", "value": 1e3 * ms, "unit": "us/call",
+        "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16-act/nvfp4-weight, bf16 MMA, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16, router rows scaled by rank^-%g)"
+                % gold["kappa"],
+        "config": {"workload": "qwen3.6-35b-a3b-shaped MoE layer prefill, T=%d tokens, H=2048 E=256 top-8 I=512 "
+                               "Is=512, skewed router (per-expert entries %d..%d), seed %d"
+                               % (T, gold["min_count"], gold["max_count"], seed),
+                   "tokens_per_step": T,
+                   "l2": "inputs larger than L2 (453 MB of NVFP4 weights per call)"},
+        "tokens_per_s": T / (ms * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak if peak else None, "peak_kind": kind, "traffic": None,
+                     "flops_per_launch": flops,
+                     "kernel": "whole step (router GEMM, top-k, expert lists, grouped tcgen05 gate/up and down "
+                               "GEMMs, combine): algorithmic FLOPs / step time"},
+        "e2e": {"value": 1e3 * e2e_ms, "unit": "us/call", "h2d_bytes_per_step": 2 * T * shape.H,
+                "d2h_bytes_per_step": 2 * T * shape.H},
+        "gpu_launches": nv.launches_per_layer_call(T, shape.H) * K,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -221,6 +317,10 @@ def main():
 
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.workload == "prefill":
+        if world > 1 and rank != 0:
+            return 0
+        return run_prefill(args, nv, wl, device)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
