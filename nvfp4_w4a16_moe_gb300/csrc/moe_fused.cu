@@ -133,7 +133,7 @@ __device__ __forceinline__ void decode_scale_pair(const uint8_t* srow, int s, fl
 // One 16-byte NVFP4 segment (32 codes, two scale blocks) of a row against 32
 // fp32 activations in the interleaved layout: s0 * sum_0..15 + s1 * sum_16..31.
 template <int KIND>
-__device__ __noinline__ float seg_dot(const uint8_t* row, const uint8_t* srow, const float4* xv, int nseg,
+__device__ __forceinline__ float seg_dot(const uint8_t* row, const uint8_t* srow, const float4* xv, int nseg,
                                       int s) {
     const uint4 w = reinterpret_cast<const uint4*>(row)[s];
     float s0, s1;
@@ -163,7 +163,7 @@ __device__ __noinline__ float seg_dot(const uint8_t* row, const uint8_t* srow, c
 // Warp task on a (gate row, up row) pair: lane `lane` takes segment 32*t + lane;
 // returns the warp-reduced (gate, up) partial dot products on every lane.
 template <int KIND>
-__device__ __noinline__ float2 pair_task(const uint8_t* grow, const uint8_t* urow, const uint8_t* gsr,
+__device__ __forceinline__ float2 pair_task(const uint8_t* grow, const uint8_t* urow, const uint8_t* gsr,
                                          const uint8_t* usr, const float4* xf, int nsegH, int t, int lane) {
     const int s = 32 * t + lane;
     float ga = 0.f, ua = 0.f;
