@@ -174,6 +174,43 @@ __device__ __forceinline__ float2 pair_task(const uint8_t* grow, const uint8_t* 
     return make_float2(warp_sum(ga), warp_sum(ua));
 }
 
+// Segment s of a gate row and an up row against the same activations (the
+// activation loads are shared): (gate, up) partial dot products.
+template <int KIND>
+__device__ __forceinline__ float2 seg_dot2(const uint8_t* grow, const uint8_t* urow, const uint8_t* gsr,
+                                           const uint8_t* usr, const float4* xv, int nseg, int s) {
+    const uint4 wg = reinterpret_cast<const uint4*>(grow)[s];
+    const uint4 wu = reinterpret_cast<const uint4*>(urow)[s];
+    float g0, g1, u0, u1;
+    decode_scale_pair<KIND>(gsr, s, g0, g1);
+    decode_scale_pair<KIND>(usr, s, u0, u1);
+    const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w}, uw[4] = {wu.x, wu.y, wu.z, wu.w};
+    float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 a = xv[(2 * q) * nseg + s];
+        const float4 b = xv[(2 * q + 1) * nseg + s];
+        const float xa[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float2 vg = e2m1x2_to_f32x2(gw[q] >> (8 * h)), vu = e2m1x2_to_f32x2(uw[q] >> (8 * h));
+            pg[q >> 1] = fmaf(vg.y, xa[2 * h + 1], fmaf(vg.x, xa[2 * h], pg[q >> 1]));
+            pu[q >> 1] = fmaf(vu.y, xa[2 * h + 1], fmaf(vu.x, xa[2 * h], pu[q >> 1]));
+        }
+    }
+    return make_float2(fmaf(g0, pg[0], g1 * pg[1]), fmaf(u0, pu[0], u1 * pu[1]));
+}
+
+// Warp sums of two values in five shuffles: lane 0 gets sum(a), lane 16 sum(b).
+__device__ __forceinline__ float warp_sum2(float a, float b, int lane) {
+    const bool lo = lane < 16;
+    float m = lo ? a : b;
+    m += __shfl_xor_sync(0xffffffffu, lo ? b : a, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    return m;
+}
+
 // Copy global bytes [begin, end) of `base` (a 16-byte aligned buffer whose length
 // is a multiple of 16) into shared memory at dst, widened to 16-byte bounds; the
 // data then starts at dst + (begin & 15). Returns the bytes requested.
@@ -443,7 +480,7 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
         __syncwarp();
         const int ch = lane >> 3, piece = (lane >> 2) & 1, pt = lane & 3;
         const int qa = q0 + nq * ch / kChunks, qb = q0 + nq * (ch + 1) / kChunks;
-        if (qb > qa) {
+        if (ch < kChunks && qb > qa) {
             const int ja = (int)fdiv(qa, P.mI);
             const int qs = piece == 0 ? qa : (ja + 1) * I;          // first row of this piece
             const int qe = piece == 0 ? min(qb, (ja + 1) * I) : qb;
@@ -479,16 +516,22 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
         }
     }
 
-    // warp tasks: (row r, segment half t), in chunk order
-    for (int task = warp; task < nq * SS; task += kFWarps) {
-        const int r = (int)fdiv(task, P.mSS);
+    // one warp per (gate, up) row pair, in chunk order: lane l takes segments l, l + 32,
+    // ...; gate and up share the activation loads and are reduced together
+    for (int r = warp; r < nq; r += kFWarps) {
         int ch = 0;
         while (ch + 1 < kChunks && r >= nq * (ch + 1) / kChunks) ++ch;
         alive = mbar_wait_bounded(&mbB[ch], 0, kDefaultWaitLimit) && alive;
-        const float2 gu = pair_task<KIND>(W + (size_t)r * rowH, W + bUP + (size_t)r * rowH, W + bGS + (size_t)r * srowH,
-                                          W + bUS + (size_t)r * srowH, xf, nsegH, task - r * SS, lane);
-        part[2 * task] = gu.x;
-        part[2 * task + 1] = gu.y;
+        float ga = 0.f, ua = 0.f;
+#pragma unroll 1
+        for (int sg = lane; sg < nsegH; sg += 32) {
+            const float2 v = seg_dot2<KIND>(W + (size_t)r * rowH, W + bUP + (size_t)r * rowH, W + bGS + (size_t)r * srowH,
+                                            W + bUS + (size_t)r * srowH, xf, nsegH, sg);
+            ga += v.x;
+            ua += v.y;
+        }
+        const float m = warp_sum2(ga, ua, lane);
+        if ((lane & 15) == 0) part[2 * r + (lane >> 4)] = m;
     }
     if (!alive) s_fail = 1;
     if (warp == 1 && lane < k) {
@@ -498,8 +541,7 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
     }
     __syncthreads();
     if (!s_fail && tid < nq) {
-        float ga = 0.f, ua = 0.f;
-        for (int t = 0; t < SS; ++t) { ga += part[2 * (tid * SS + t)]; ua += part[2 * (tid * SS + t) + 1]; }
+        const float ga = part[2 * tid], ua = part[2 * tid + 1];
         const int q = q0 + tid, j = (int)fdiv(q, P.mI);
         st_word(w_h + j * I + il_pos(q - j * I, nsegI), tag, silu_f32(ga * s_tsg[j]) * (ua * s_tsu[j]));
     }
@@ -538,31 +580,25 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
         return;
     }
     {
-        // warp tasks: (output row nl, group of 32 (slot, segment) pairs); slot k is the shared expert
+        // one warp per output row nl: lane l takes the (slot, segment) pairs l, l + 32, ...
+        // (slot k is the shared expert), accumulates all their weighted dot products and
+        // the warp is reduced once
         const float4* hsm = reinterpret_cast<const float4*>(W);
-        const int work_r = k * nsegI, work = work_r + nsegS;
-        const int GC = (work + 31) / 32;
-        for (int task = warp; task < nN * GC; task += kFWarps) {
-            const int nl = (int)fdiv(task, P.mGC);
-            const int p = 32 * (task - nl * GC) + lane;
+        const int work = k * nsegI + nsegS;
+        for (int nl = warp; nl < nN; nl += kFWarps) {
             float acc = 0.f;
-            if (p < work) {
-                int j = 0, s = p;
-                while (j < k && s >= nsegI) { s -= nsegI; ++j; }
+#pragma unroll 1
+            for (int p = lane; p < work; p += 32) {
+                int j = 0, sg = p;
+                while (j < k && sg >= nsegI) { sg -= nsegI; ++j; }
                 const bool sh = j == k;
                 const uint8_t* row = D + (size_t)j * P.dn_stride + (size_t)nl * (sh ? rowS : rowI);
                 const uint8_t* srow = DS + (size_t)j * P.dns_stride + (sh ? sh_soff + (size_t)nl * srowS
                                                                           : r_soff + (size_t)nl * srowI);
-                acc = s_coef[j] * seg_dot<KIND>(row, srow, hsm + j * (I >> 2), sh ? nsegS : nsegI, s);
+                acc = fmaf(s_coef[j], seg_dot<KIND>(row, srow, hsm + j * (I >> 2), sh ? nsegS : nsegI, sg), acc);
             }
             acc = warp_sum(acc);
-            if (lane == 0) part[task] = acc;
-        }
-        __syncthreads();
-        if (tid < nN) {
-            float acc = 0.f;
-            for (int g = 0; g < GC; ++g) acc += part[tid * GC + g];
-            P.y[n0 + tid] = f32_to_bf16(acc);
+            if (lane == 0) P.y[n0 + nl] = f32_to_bf16(acc);
         }
     }
 }
