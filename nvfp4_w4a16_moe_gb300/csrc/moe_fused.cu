@@ -70,7 +70,7 @@ struct FusedParams {
     uint32_t dn_stride;   // bytes per expert slot in the packed down region
     uint32_t dns_stride;  // bytes per expert slot in the down-scale region
     // ceil(2^32 / d) for the divisors used on the device (exact for the ranges used)
-    unsigned long long mG, mI, mRS, mSS, mGC;
+    unsigned long long mG, mI;
     unsigned long long mG64;   // ceil(2^64 / G)
 };
 
@@ -160,19 +160,6 @@ __device__ __forceinline__ float seg_dot(const uint8_t* row, const uint8_t* srow
     return fmaf(s0, p[0], s1 * p[1]);
 }
 
-// Warp task on a (gate row, up row) pair: lane `lane` takes segment 32*t + lane;
-// returns the warp-reduced (gate, up) partial dot products on every lane.
-template <int KIND>
-__device__ __forceinline__ float2 pair_task(const uint8_t* grow, const uint8_t* urow, const uint8_t* gsr,
-                                         const uint8_t* usr, const float4* xf, int nsegH, int t, int lane) {
-    const int s = 32 * t + lane;
-    float ga = 0.f, ua = 0.f;
-    if (s < nsegH) {
-        ga = seg_dot<KIND>(grow, gsr, xf, nsegH, s);
-        ua = seg_dot<KIND>(urow, usr, xf, nsegH, s);
-    }
-    return make_float2(warp_sum(ga), warp_sum(ua));
-}
 
 // Segment s of a gate row and an up row against the same activations (the
 // activation loads are shared): (gate, up) partial dot products.
@@ -292,8 +279,6 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
     const int nS = Is > cs ? (int)fdiv(Is - 1 - cs, P.mG) + 1 : 0;
     const int n0 = (int)fdiv(H * c, P.mG), n1 = (int)fdiv(H * (c + 1), P.mG);
     const int nN = n1 - n0;
-    const int RS = (nchH + 31) / 32;       // warp tasks per router row (32 chunks each)
-    const int SS = (nsegH + 31) / 32;      // warp tasks per NVFP4 row of K = H (32 segments each)
     // phase-A region: [router rows nR x 2H][pairs: gate row, up row, gate scales, up scales]
     const uint32_t aPair = (uint32_t)nR * 2 * H;
     const uint32_t pairBytes = 2u * (rowH + srowH);
@@ -367,41 +352,32 @@ __global__ void __launch_bounds__(kFThreads, 2) moe_decode_t1_kernel(FusedParams
     const uint32_t tag = s_tag;
 
     // ---------------------------------------------------------------- phase A
-    // warp tasks: router row j part t (32 chunks of 8 bf16), shared pair j half t
+    // one warp per router row (lanes over its chunks of 8 bf16) and one per shared-expert
+    // (gate, up) row pair (lanes over its segments); each is reduced once
     bool alive = copies_done(&mbA, P.hdr);
-    const int nTA = nR * RS + nS * SS;
     if (alive) {
-        for (int task = warp; task < nTA; task += kFWarps) {
-            if (task < nR * RS) {
-                const int j = (int)fdiv(task, P.mRS), ch = 32 * (task - j * RS) + lane;
-                const float acc = ch < nchH ? bf16_chunk_dot(reinterpret_cast<const uint4*>(W + (size_t)j * 2 * H)[ch], xb[ch], 0.f) : 0.f;
-                part[2 * task] = warp_sum(acc);
+        for (int task = warp; task < nR + nS; task += kFWarps) {
+            if (task < nR) {
+                const uint4* wr = reinterpret_cast<const uint4*>(W + (size_t)task * 2 * H);
+                float acc = 0.f;
+#pragma unroll 1
+                for (int ch = lane; ch < nchH; ch += 32) acc = bf16_chunk_dot(wr[ch], xb[ch], acc);
+                acc = warp_sum(acc);
+                if (lane == 0) st_word(w_lg + c + G * task, tag, acc);   // row E: the gate pre-activation
             } else {
-                const int tt = task - nR * RS, j = (int)fdiv(tt, P.mSS);
+                const int j = task - nR, p = cs + G * j;
                 const uint8_t* pr = W + aPair + (size_t)j * pairBytes;
-                const float2 gu = pair_task<KIND>(pr, pr + rowH, pr + 2 * rowH, pr + 2 * rowH + srowH, xf, nsegH,
-                                                  tt - j * SS, lane);
-                part[2 * task] = gu.x;
-                part[2 * task + 1] = gu.y;
+                float ga = 0.f, ua = 0.f;
+#pragma unroll 1
+                for (int sg = lane; sg < nsegH; sg += 32) {
+                    const float2 v = seg_dot2<KIND>(pr, pr + rowH, pr + 2 * rowH, pr + 2 * rowH + srowH, xf, nsegH, sg);
+                    ga += v.x;
+                    ua += v.y;
+                }
+                const float m = warp_sum2(ga, ua, lane);
+                const float gsum = __shfl_sync(0xffffffffu, m, 0), usum = __shfl_sync(0xffffffffu, m, 16);
+                if (lane == 0) st_word(w_h + total + il_pos(p, nsegS), tag, silu_f32(gsum * sh_tsg) * (usum * sh_tsu));
             }
-        }
-    }
-    __syncthreads();
-    if (alive) {
-        if (tid < nR) {
-            float acc = 0.f;
-            for (int t = 0; t < RS; ++t) acc += part[2 * (tid * RS + t)];
-            st_word(w_lg + c + G * tid, tag, acc);           // row E: the gate pre-activation
-        } else if (tid >= 32 && tid < 32 + nS) {
-            const int j = tid - 32, p = cs + G * j;
-            float ga = 0.f, ua = 0.f;
-            for (int t = 0; t < SS; ++t) {
-                const int task = nR * RS + j * SS + t;
-                ga += part[2 * task];
-                ua += part[2 * task + 1];
-            }
-            const float hv = silu_f32(ga * sh_tsg) * (ua * sh_tsu);
-            st_word(w_h + total + il_pos(p, nsegS), tag, hv);
         }
     }
     // the next launch on the stream may start its weight-only prologue now
@@ -634,12 +610,8 @@ FusedLayout fused_layout(const moe_layer_desc& d, int G) {
     L.off_w = (uint32_t)off; off += up16(w);
     L.off_d = (uint32_t)off; off += (size_t)L.dn_stride * (k + 1);
     L.off_ds = (uint32_t)off; off += (size_t)L.dns_stride * (k + 1);
-    // per-task partial sums (floats): phase A 2*(nR*RS + nS*SS), phase B 2*nq*SS, phase C nN*GC
-    const size_t RS = (H / 8 + 31) / 32, SS = (H / 32 + 31) / 32;
-    const size_t GC = (k * (I / 32) + Is / 32 + 31) / 32;
-    size_t np = 2 * (nR * RS + nS * SS);
-    if (2 * nq * SS > np) np = 2 * nq * SS;
-    if (nN * GC > np) np = nN * GC;
+    // phase-B (gate, up) sums of the block's row pairs
+    const size_t np = 2 * nq;
     L.off_part = (uint32_t)off; off += up16(np * 4);
     L.total = (uint32_t)off;
     return L;
@@ -676,13 +648,8 @@ cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, 
     P.dn_stride = L.dn_stride;
     P.dns_stride = L.dns_stride;
     auto magic = [](uint32_t dv) { return ((1ull << 32) + dv - 1) / dv; };
-    const uint32_t RS = (uint32_t)(d.H / 8 + 31) / 32, SS = (uint32_t)(d.H / 32 + 31) / 32;
-    const uint32_t GC = (uint32_t)(d.k * (d.I / 32) + d.Is / 32 + 31) / 32;
     P.mG = magic(G);
     P.mI = magic(d.I);
-    P.mRS = magic(RS);
-    P.mSS = magic(SS);
-    P.mGC = magic(GC);
     P.mG64 = ~0ull / (unsigned long long)G + 1ull;
     auto kern = d.kind == NVFP4_SCALE_E4M3 ? moe_decode_t1_kernel<NVFP4_SCALE_E4M3>
                                            : moe_decode_t1_kernel<NVFP4_SCALE_FP16>;
