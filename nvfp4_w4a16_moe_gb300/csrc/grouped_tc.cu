@@ -95,11 +95,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)) : "memory");
 }
 
-// Bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-    if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
-
 // generic-proxy writes to shared memory -> visible to the tensor cores' async proxy
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -387,25 +382,6 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
         for (int j = 0; j < 16; ++j) {
             const int src = tok[(lt >> 3) + 16 * j];
             boff[j] = src < 0 ? -1 : src * P.H + bc * 8;
-        }
-        if (lt == 0) {
-            // the CTA reads its weight rows once, over the whole K loop: start them all
-            // towards L2 now
-            if (kMode == 0) {
-                const int rows = min(kM, Fvalid - feat0);
-                const uint8_t* pk = shared ? P.sh_gu_packed : P.gu_packed;
-                const uint8_t* sc = shared ? P.sh_gu_scales : P.gu_scales;
-                bulk_prefetch_l2(pk + (size_t)y0 * (P.H / 2), (uint32_t)rows * (P.H / 2));
-                bulk_prefetch_l2(pk + (size_t)y1 * (P.H / 2), (uint32_t)rows * (P.H / 2));
-                bulk_prefetch_l2(sc + (size_t)y0 * (P.H / 16), (uint32_t)rows * (P.H / 16));
-                bulk_prefetch_l2(sc + (size_t)y1 * (P.H / 16), (uint32_t)rows * (P.H / 16));
-            } else {
-                const int rows = min(kRows, P.H - feat0);
-                const uint8_t* pk = shared ? P.sh_dn_packed : P.dn_packed;
-                const uint8_t* sc = shared ? P.sh_dn_scales : P.dn_scales;
-                bulk_prefetch_l2(pk + (size_t)y0 * (Kd / 2), (uint32_t)rows * (Kd / 2));
-                bulk_prefetch_l2(sc + (size_t)y0 * (Kd / 16), (uint32_t)rows * (Kd / 16));
-            }
         }
         if (kMode == 0 || lt == 0) {
             int st = 0, use = 0;   // ring slot of step s and how many times it was filled before
