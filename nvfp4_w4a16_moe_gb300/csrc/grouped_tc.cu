@@ -20,18 +20,25 @@
 // small experts waste no MMA work on padding and each weight tile is expanded once
 // for up to 256 tokens.
 //
-// Warp roles per CTA (416 threads), ring of S stages:
-//   warps 8-11 (loaders): for step s, wait until the MMAs of step s - S are done,
-//     cp.async the token rows into the 128-byte-swizzled B tile and the raw NVFP4
-//     bytes of the weight rows into a staging area, then let the copies themselves
-//     arrive on full_ld[s % S] (cp.async.mbarrier.arrive.noinc);
-//   warps 0-7 (expanders): wait on full_ld, expand the NVFP4 bytes into the
-//     swizzled bf16 A tile, fence to the async proxy, arrive on full_a;
-//   warp 12 (one lane): wait on full_ld and full_a, issue the MMAs, commit them to
-//     empty[s % S]; after the last step, commit to the accumulator barrier;
-//   warps 0-7 then read TMEM, run the epilogue through shared memory and store
-//     coalesced rows. Every wait is bounded; a wait that runs out records
-// NVFP4_ERR_DEVICE_TIMEOUT and makes every later wait of the CTA give up at once.
+// Warp roles per CTA (704 threads) and three rings that move at their own pace:
+//   warp 16, one lane (raw stream): for step s, wait until the expanders have read
+//     the raw slot of step s - R, then TMA the step's NVFP4 codes and block scales of
+//     the 256 weight rows into it (R = 5..8 slots: the HBM-latency stream runs far
+//     ahead);
+//   warps 17-20 (token stream): for step s, wait until the MMAs of step s - SB are
+//     done, then bring the tile's token rows into the 128-byte-swizzled B slot
+//     (gate/up: gathered rows of x by cp.async, whose completion arrives on the slot's
+//     barrier; down: contiguous rows of h / hs by TMA);
+//   warps 0-15 (expanders): wait for the raw slot, read it, release it, wait for a
+//     free A slot (two), expand the NVFP4 bytes into the swizzled bf16 A tile, fence
+//     to the async proxy and arrive;
+//   warp 21, one lane: wait for the A and B slots of step s, issue the MMAs and
+//     commit them to both slots' empty barriers; after the last step, commit to the
+//     accumulator barrier;
+//   warps 0-15 then read TMEM, run the epilogue through shared memory and store
+//     coalesced rows.
+// Every wait is bounded; a wait that runs out records NVFP4_ERR_DEVICE_TIMEOUT and
+// makes every later wait of the CTA give up at once.
 //
 // NVFP4 -> bf16 expansion (exact): cvt.rn.f16x2.e2m1x2 gives the E2M1 values as
 // f16; shifting an f16 bit pattern right by 3 (sign kept in place) reads it as a
@@ -55,15 +62,19 @@ constexpr int kM = 128;           // weight rows per accumulator (MMA M)
 constexpr int kKS = 64;           // K elements per stage: one 128-byte row of the swizzle atom
 constexpr int kRows = 2 * kM;     // weight rows per CTA: two accumulators share the token tile
 constexpr int kExp = 512;         // expander / epilogue threads (warps 0-15): half a weight row each
-constexpr int kLd = 128;          // operand loader threads (warps 16-19)
-constexpr int kMmaWarp = (kExp + kLd) / 32;   // warp 20: TMEM owner and MMA issuer
-constexpr int kTcThreads = kExp + kLd + 32;
-constexpr int kMaxStages = 8;
+constexpr int kRawWarp = kExp / 32;           // warp 16, lane 0: weight codes and scales (TMA)
+constexpr int kBWarp0 = kRawWarp + 1;         // warps 17-20: token rows (cp.async; the down GEMM: TMA by lane 0)
+constexpr int kBThreads = 128;
+constexpr int kMmaWarp = kBWarp0 + kBThreads / 32;   // warp 21: TMEM owner and MMA issuer
+constexpr int kTcThreads = (kMmaWarp + 1) * 32;
+constexpr int kMaxRaw = 8;        // raw weight ring depth (at most)
+constexpr int kMaxB = 4;          // token-row ring depth (at most)
 
-// Dynamic shared memory: [1024-byte alignment slack][stage ring][fixed tables]. A
-// stage holds the bf16 A tile (kRows x 64, swizzled), the bf16 B tile (N x 64,
-// swizzled; N = the tile's token count rounded up to 16) and the raw NVFP4 bytes
-// of the A rows (TMA boxes); the number of stages follows from N.
+// Dynamic shared memory: [1024-byte alignment slack][rings][fixed tables]. Three rings
+// move at their own pace: the raw NVFP4 bytes of the A rows (TMA boxes from HBM, the
+// longest latency: the deepest ring), the bf16 token rows (N x 64, 128-byte swizzled;
+// N = the tile's token count rounded up to 16), and the expanded bf16 A tile (two
+// slots: one being expanded while the MMAs read the other).
 constexpr int kA = kRows * 128;
 constexpr int kRawScales = kRows * 32;      // raw: codes [kRows][32 B], then scales [kRows][16 B]
 constexpr int kRawStage = kRows * 48;       // (the 16 scale bytes hold 4 K steps; step s uses bytes 4(s%4)..)
@@ -71,7 +82,8 @@ constexpr int kRing = 220 * 1024;
 constexpr int kOffTok = kRing;                          // per token row: source row (-1: none)
 constexpr int kOffCols = kOffTok + kTokTile * 4;        // per token column: (Y row, scale)
 constexpr int kOffBar = kOffCols + kTokTile * 8;
-constexpr int kSmemBytes = 1024 + kOffBar + (3 * kMaxStages + 1) * 8 + 16;
+constexpr int kNumBars = 2 * kMaxRaw + 2 * kMaxB + 4 + 1;
+constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;   // TMEM column offset of the second accumulator
 
@@ -276,14 +288,19 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
     const int Kd = kMode == 0 ? P.H : (shared ? P.Is : P.I);
     const int nk = Kd / kKS;
     const int N = (tr.n_rows + 15) & ~15;
-    const int stage_bytes = kA + N * 128 + kRawStage;   // multiple of 1024
-    const int S = min(kMaxStages, kRing / stage_bytes);
+    const int bbytes = N * 128;                                      // one token-row stage (multiple of 2048)
+    const int SB = N > 128 ? 3 : kMaxB;                              // token-row ring depth
+    const int R = min(kMaxRaw, (kRing - 2 * kA - SB * bbytes) / kRawStage);   // raw weight ring depth
+    const uint32_t offB = 2 * kA, offRaw = offB + SB * bbytes;       // ring offsets (multiples of 1024)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    uint64_t* full_ld = reinterpret_cast<uint64_t*>(sm + kOffBar);   // B rows and raw weights landed
-    uint64_t* full_a = full_ld + kMaxStages;                          // A tile expanded
-    uint64_t* empty = full_a + kMaxStages;                            // MMAs of the stage done
-    uint64_t* accb = empty + kMaxStages;                              // all MMAs done
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + kOffBar);   // raw weight bytes landed (TMA)
+    uint64_t* raw_empty = raw_full + kMaxRaw;                          // raw slot read by the expanders
+    uint64_t* b_full = raw_empty + kMaxRaw;                            // token rows landed
+    uint64_t* b_empty = b_full + kMaxB;                                // MMAs done with the token rows
+    uint64_t* a_full = b_empty + kMaxB;                                // [2] A tile expanded
+    uint64_t* a_empty = a_full + 2;                                    // [2] MMAs done with the A tile
+    uint64_t* accb = a_empty + 2;                                      // all MMAs done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* tok = reinterpret_cast<int*>(sm + kOffTok);
@@ -291,10 +308,17 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
 
     if (warp == kMmaWarp) {
         if (lane == 0) {
-            for (int i = 0; i < S; ++i) {
-                mbar_init(&full_ld[i], kMode == 0 ? kLd + 1 : 1);
-                mbar_init(&full_a[i], kExp);
-                mbar_init(&empty[i], 1);
+            for (int i = 0; i < R; ++i) {
+                mbar_init(&raw_full[i], 1);
+                mbar_init(&raw_empty[i], kExp);
+            }
+            for (int i = 0; i < SB; ++i) {
+                mbar_init(&b_full[i], kMode == 0 ? kBThreads : 1);
+                mbar_init(&b_empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&a_full[i], kExp);
+                mbar_init(&a_empty[i], 1);
             }
             mbar_init(accb, 1);
             *abort_flag = 0;
@@ -356,66 +380,74 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
         }
     };
 
-    if (warp >= kExp / 32 && warp < kMmaWarp) {
-        // ---------------- loaders: weight codes and scales (TMA, one thread), token rows
-        // (gate/up: gathered rows of x by cp.async from all loader threads; down: the
-        // tile's contiguous rows of h / hs by TMA)
-        const int lt = tid - kExp;
-        const CUtensorMap* mc = kMode == 0 ? (shared ? &maps.sh_gu_codes : &maps.gu_codes)
-                                           : (shared ? &maps.sh_dn_codes : &maps.dn_codes);
-        const CUtensorMap* ms = kMode == 0 ? (shared ? &maps.sh_gu_scales : &maps.gu_scales)
-                                           : (shared ? &maps.sh_dn_scales : &maps.dn_scales);
-        int y0, y1;   // first weight row of A rows 0-127 and 128-255
-        if (kMode == 0) {
-            const int base = shared ? 0 : tr.slot * 2 * P.I;
-            y0 = base + feat0;
-            y1 = base + Fvalid + feat0;
-        } else {
-            y0 = (shared ? 0 : tr.slot * P.H) + feat0;
-            y1 = y0 + kM;
-        }
-        const uint32_t tx = 2 * (32 * kM) + 2 * (16 * kM) + (kMode == 1 ? N * 128 : 0);
-        const uint16_t* bsrc = P.x;
-        const int bc = lt & 7;
-        int boff[16];   // gate/up: element offset of this thread's chunk in row (lt >> 3) + 16 j, or -1
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int src = tok[(lt >> 3) + 16 * j];
-            boff[j] = src < 0 ? -1 : src * P.H + bc * 8;
-        }
-        if (kMode == 0 || lt == 0) {
-            int st = 0, use = 0;   // ring slot of step s and how many times it was filled before
+    if (warp == kRawWarp) {
+        // ---------------- raw weight stream (one thread): codes and scales of the A rows,
+        // up to R steps ahead of the expanders
+        if (lane == 0) {
+            const CUtensorMap* mc = kMode == 0 ? (shared ? &maps.sh_gu_codes : &maps.gu_codes)
+                                               : (shared ? &maps.sh_dn_codes : &maps.dn_codes);
+            const CUtensorMap* ms = kMode == 0 ? (shared ? &maps.sh_gu_scales : &maps.gu_scales)
+                                               : (shared ? &maps.sh_dn_scales : &maps.dn_scales);
+            int y0, y1;   // first weight row of A rows 0-127 and 128-255
+            if (kMode == 0) {
+                const int base = shared ? 0 : tr.slot * 2 * P.I;
+                y0 = base + feat0;
+                y1 = base + Fvalid + feat0;
+            } else {
+                y0 = (shared ? 0 : tr.slot * P.H) + feat0;
+                y1 = y0 + kM;
+            }
 #pragma unroll 1
             for (int s = 0; s < nk; ++s) {
-                if (use > 0) wait_or_abort(&empty[st], (use - 1) & 1, abort_flag, hdr, wait_limit);
-                const uint32_t stage = sm_base + st * stage_bytes;
-                const uint32_t bt = stage + kA;
-                const uint32_t raw = bt + N * 128;
-                if (lt == 0) {
-                    mbar_arrive_expect_tx(&full_ld[st], tx);
-                    tma_load_2d(raw, mc, s * 32, y0, &full_ld[st]);
-                    tma_load_2d(raw + kM * 32, mc, s * 32, y1, &full_ld[st]);
-                    tma_load_2d(raw + kRawScales, ms, (s >> 2) * 16, y0, &full_ld[st]);
-                    tma_load_2d(raw + kRawScales + kM * 16, ms, (s >> 2) * 16, y1, &full_ld[st]);
-                    if (kMode == 1) {
-                        const CUtensorMap* mb = shared ? &maps.hs : &maps.h;
-                        for (int i = 0; i < N / kBoxRowsB; ++i)
-                            tma_load_2d(bt + i * (kBoxRowsB * 128), mb, s * kKS, tr.p0 + i * kBoxRowsB, &full_ld[st]);
-                    }
-                }
-                if (kMode == 0) {
+                const int r = s % R, u = s / R;
+                if (u > 0) wait_or_abort(&raw_empty[r], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                const uint32_t raw = sm_base + offRaw + r * kRawStage;
+                mbar_arrive_expect_tx(&raw_full[r], 2 * (32 * kM) + 2 * (16 * kM));
+                tma_load_2d(raw, mc, s * 32, y0, &raw_full[r]);
+                tma_load_2d(raw + kM * 32, mc, s * 32, y1, &raw_full[r]);
+                tma_load_2d(raw + kRawScales, ms, (s >> 2) * 16, y0, &raw_full[r]);
+                tma_load_2d(raw + kRawScales + kM * 16, ms, (s >> 2) * 16, y1, &raw_full[r]);
+            }
+        }
+    } else if (warp >= kBWarp0 && warp < kMmaWarp) {
+        // ---------------- token-row stream, up to SB steps ahead of the MMAs (gate/up:
+        // gathered rows of x by cp.async from 128 threads; down: the tile's contiguous
+        // rows of h / hs by TMA from one thread)
+        const int bt = tid - kBWarp0 * 32;
+        if (kMode == 0) {
+            const int bc = bt & 7;
+            int boff[16];   // element offset of this thread's chunk in row (bt >> 3) + 16 j, or -1
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int row = (lt >> 3) + 16 * j;
-                        if (row < N) {
-                            const uint32_t dst = bt + row * 128 + ((bc ^ (row & 7)) << 4);
-                            if (boff[j] >= 0) cp_async16_zfill(dst, bsrc + boff[j] + s * kKS, 16u);
-                            else cp_async16_zfill(dst, P.x, 0u);
-                        }
+            for (int j = 0; j < 16; ++j) {
+                const int src = tok[(bt >> 3) + 16 * j];
+                boff[j] = src < 0 ? -1 : src * P.H + bc * 8;
+            }
+#pragma unroll 1
+            for (int s = 0; s < nk; ++s) {
+                const int b = s % SB, u = s / SB;
+                if (u > 0) wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                const uint32_t bb = sm_base + offB + b * bbytes;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int row = (bt >> 3) + 16 * j;
+                    if (row < N) {
+                        const uint32_t dst = bb + row * 128 + ((bc ^ (row & 7)) << 4);
+                        if (boff[j] >= 0) cp_async16_zfill(dst, P.x + boff[j] + s * kKS, 16u);
+                        else cp_async16_zfill(dst, P.x, 0u);
                     }
-                    cp_async_arrive_noinc(&full_ld[st]);
                 }
-                if (++st == S) { st = 0; ++use; }
+                cp_async_arrive_noinc(&b_full[b]);
+            }
+        } else if (bt == 0) {
+            const CUtensorMap* mb = shared ? &maps.hs : &maps.h;
+#pragma unroll 1
+            for (int s = 0; s < nk; ++s) {
+                const int b = s % SB, u = s / SB;
+                if (u > 0) wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                const uint32_t bb = sm_base + offB + b * bbytes;
+                mbar_arrive_expect_tx(&b_full[b], (uint32_t)bbytes);
+                for (int i = 0; i < N / kBoxRowsB; ++i)
+                    tma_load_2d(bb + i * (kBoxRowsB * 128), mb, s * kKS, tr.p0 + i * kBoxRowsB, &b_full[b]);
             }
         }
     } else if (warp < kExp / 32) {
@@ -427,16 +459,21 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
         const bool valid = rcode != nullptr;
         const int rl = r & 7;   // swizzle phase of the row
         const int a_off = (r >> 7) * (kM * 128) + (r & (kM - 1)) * 128;
-        int st = 0, ph = 0;
 #pragma unroll 1
         for (int kt = 0; kt < nk; ++kt) {
-            wait_or_abort(&full_ld[st], ph, abort_flag, hdr, wait_limit);
-            uint8_t* stage = sm + st * stage_bytes;
-            uint8_t* arow = stage + a_off;
-            const uint8_t* raw = stage + kA + N * 128;
+            const int rr = kt % R, a = kt & 1;
+            wait_or_abort(&raw_full[rr], (kt / R) & 1, abort_flag, hdr, wait_limit);
+            const uint8_t* raw = sm + offRaw + rr * kRawStage;
+            uint4 c0 = make_uint4(0, 0, 0, 0);
+            uint32_t sw = 0;
             if (valid) {
-                const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 32 + half * 16);
-                const uint32_t sw = *reinterpret_cast<const uint32_t*>(raw + kRawScales + r * 16 + (kt & 3) * 4);
+                c0 = *reinterpret_cast<const uint4*>(raw + r * 32 + half * 16);
+                sw = *reinterpret_cast<const uint32_t*>(raw + kRawScales + r * 16 + (kt & 3) * 4);
+            }
+            mbar_arrive(&raw_empty[rr]);   // the raw slot may be refilled
+            if (kt >= 2) wait_or_abort(&a_empty[a], ((kt >> 1) - 1) & 1, abort_flag, hdr, wait_limit);
+            uint8_t* arow = sm + a * kA + a_off;
+            if (valid) {
                 uint32_t s0, s1;
                 scale_pair_bf16(sw >> (16 * half), s0, s1);
                 const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
@@ -452,8 +489,7 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
                     *reinterpret_cast<uint4*>(arow + ((4 * half + c) << 4)) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&full_a[st]);
-            if (++st == S) { st = 0; ph ^= 1; }
+            mbar_arrive(&a_full[a]);
         }
 
         // ---------------- epilogue: TMEM -> registers -> shared staging -> global
@@ -516,29 +552,29 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
             }
             tc_fence_before();
         }
-    } else if (lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
         // ---------------- MMA issuer (one thread)
         const uint32_t idesc = f16_idesc(kM, N);
-        int st = 0, ph = 0;
 #pragma unroll 1
         for (int kt = 0; kt < nk; ++kt) {
-            if (!wait_or_abort(&full_ld[st], ph, abort_flag, hdr, wait_limit)) break;
-            if (!wait_or_abort(&full_a[st], ph, abort_flag, hdr, wait_limit)) break;
-            // the B rows were written by cp.async (generic proxy): order them before the
-            // tensor cores' reads
+            const int a = kt & 1, b = kt % SB;
+            if (!wait_or_abort(&a_full[a], (kt >> 1) & 1, abort_flag, hdr, wait_limit)) break;
+            if (!wait_or_abort(&b_full[b], (kt / SB) & 1, abort_flag, hdr, wait_limit)) break;
+            // the token rows may have been written by cp.async (generic proxy): order them
+            // before the tensor cores' reads
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t stage = sm_base + st * stage_bytes;
+            const uint32_t abase = sm_base + a * kA, bbase = sm_base + offB + b * bbytes;
 #pragma unroll
             for (int j = 0; j < kKS / 16; ++j) {
-                const uint64_t bd = sw128_desc(stage + kA + j * 32);
+                const uint64_t bd = sw128_desc(bbase + j * 32);
 #pragma unroll
                 for (int p = 0; p < 2; ++p)
-                    tc_mma(tmem + p * kAccStride, sw128_desc(stage + p * (kM * 128) + j * 32), bd, idesc,
+                    tc_mma(tmem + p * kAccStride, sw128_desc(abase + p * (kM * 128) + j * 32), bd, idesc,
                            (kt | j) != 0);
             }
-            tc_commit(&empty[st]);
-            if (++st == S) { st = 0; ph ^= 1; }
+            tc_commit(&a_empty[a]);
+            tc_commit(&b_empty[b]);
         }
         tc_commit(accb);
     }
