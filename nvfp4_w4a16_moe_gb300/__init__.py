@@ -25,18 +25,18 @@ SCALE_E4M3 = 0
 SCALE_FP16 = 1
 
 
-def launches_per_layer_call(T: int, H: int = 2048, kind: int = 0, shared: bool = True) -> int:
+def launches_per_layer_call(T: int, H: int = 2048, kind: int = 0, shared: bool = True, E: int = 256) -> int:
     """Kernel launches one moe_layer_forward call enqueues (routing outputs not requested):
     one for the single-token fused kernel, five for the multi-token decode path (per
     64-token chunk for FP16-scaled layers above 64 tokens), and for the prefill path
-    router, gate, top-k, three list passes, gate/up, down and combine (no gate launch
-    without a shared expert)."""
+    router (and the sum of its K-split partials), gate, top-k, three list passes,
+    gate/up, down and combine (no gate launch without a shared expert)."""
     if T == 1 and H % 256 == 0 and H <= 2048:
         return 1
     if T <= 64:
         return 5
     if kind == 0:
-        return 9 if shared else 8
+        return (9 if shared else 8) + (1 if (H // 32) % 2 == 0 and (T * E) % 4 == 0 else 0)
     return 5 * ((T + 63) // 64)
 
 STATUS = {

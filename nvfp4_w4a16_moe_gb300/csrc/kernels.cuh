@@ -98,7 +98,7 @@ struct PrefillWs {
 bool prefill_supported(const moe_layer_desc& d, int T);
 size_t prefill_ws_bytes(const moe_layer_desc& d, int T);
 PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T);
-int prefill_launch_count(const moe_layer_desc& d);
+int prefill_launch_count(const moe_layer_desc& d, int T);
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
                                cudaStream_t s);

@@ -186,26 +186,28 @@ __device__ __forceinline__ int acc_col(int j, int q) {
 }
 
 // ------------------------------------------------------------------ kernels
-// 1. router: logits[t, e] = x[t] . Wg[e] as one bf16 GEMM;
-//    grid = (ceil(T/128), ceil(E/128)).
+// 1. router: logits[t, e] = x[t] . Wg[e] as one bf16 GEMM, K split in blockIdx.z parts
+//    of kc elements (each writes its own partial slice; router_sum_kernel adds them in a
+//    fixed order); grid = (ceil(T/128), ceil(E/128), splits).
 __global__ void __launch_bounds__(kGThreads) router_gemm_kernel(const uint16_t* __restrict__ x, int T, int H,
-                                                              const uint16_t* __restrict__ wg, int E,
+                                                              const uint16_t* __restrict__ wg, int E, int kc,
                                                               float* __restrict__ logits) {
     extern __shared__ __align__(128) uint16_t gsm[];
     uint16_t* As = gsm;
     uint16_t* Bs = gsm + 2 * kBM * kLds;
-    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN, k0 = blockIdx.z * kc;
     const int tid = threadIdx.x;
+    logits += (size_t)blockIdx.z * T * E;
     TileSrc S{};
     S.dummy = x;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int r = (tid >> 2) + 64 * c;
-        S.a[c] = m0 + r < T ? x + (size_t)(m0 + r) * H : nullptr;
-        S.bh[c] = n0 + r < E ? wg + (size_t)(n0 + r) * H : nullptr;
+        S.a[c] = m0 + r < T ? x + (size_t)(m0 + r) * H + k0 : nullptr;
+        S.bh[c] = n0 + r < E ? wg + (size_t)(n0 + r) * H + k0 : nullptr;
     }
     float acc[4][4][4];
-    gemm_tile<false>(S, H, acc, As, Bs);
+    gemm_tile<false>(S, kc, acc, As, Bs);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -215,6 +217,19 @@ __global__ void __launch_bounds__(kGThreads) router_gemm_kernel(const uint16_t* 
                 const int r = acc_row(i, q), c = acc_col(j, q);
                 if (m0 + r < T && n0 + c < E) logits[(size_t)(m0 + r) * E + n0 + c] = acc[i][j][q];
             }
+}
+
+// logits = sum of the router's K-split partial slices, in split order (in place in slice 0).
+__global__ void router_sum_kernel(float* __restrict__ logits, int n4, int splits, size_t slice4) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4* p = reinterpret_cast<float4*>(logits);
+    float4 a = p[i];
+    for (int sp = 1; sp < splits; ++sp) {
+        const float4 v = p[i + sp * slice4];
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    p[i] = a;
 }
 
 // The gate pre-activation sigma_t = x_t . gs for every token (one warp per token).
@@ -352,6 +367,14 @@ size_t align256p(size_t v) { return (v + 255) & ~size_t(255); }
 // The grouped tcgen05 GEMMs read the weights through TMA tensor maps whose row
 // strides (K/16 bytes for the scales) must be multiples of 16: H, I and Is
 // multiples of 256, E4M3 scales (their products with E2M1 values are exact in bf16).
+// K splits of the router GEMM (so that its grid covers the SMs at 4096 tokens); each split
+// is a multiple of the 32-element K step, and the partial slices must stay 16-byte
+// aligned for the float4 sum (T*E a multiple of 4).
+int router_splits(int H, int T, int E) {
+    if (((size_t)T * E) % 4 != 0) return 1;
+    return (H / 32) % 4 == 0 ? 4 : ((H / 32) % 2 == 0 ? 2 : 1);
+}
+
 bool prefill_supported(const moe_layer_desc& d, int T) {
     return T > NVFP4_DECODE_MAX_TOKENS && d.kind == NVFP4_SCALE_E4M3 && d.H % 256 == 0 && d.I % 256 == 0 &&
            d.Is % 256 == 0;
@@ -361,7 +384,7 @@ size_t prefill_ws_bytes(const moe_layer_desc& d, int T) {
     const size_t Tk = (size_t)T * d.k;
     const size_t nb = (Tk + kLB - 1) / kLB;
     size_t b = sizeof(WsHeader);
-    b += align256p(sizeof(float) * (size_t)T * d.E);            // logits
+    b += align256p(sizeof(float) * (size_t)T * d.E * router_splits(d.H, T, d.E));   // logits (split partials)
     b += align256p(sizeof(float) * (size_t)T);                  // gate
     b += align256p(sizeof(int32_t) * Tk);                       // ids
     b += align256p(sizeof(float) * Tk);                         // w
@@ -382,7 +405,7 @@ PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T) {
     char* p = static_cast<char*>(base);
     auto take = [&](size_t bytes) { char* r = p; p += align256p(bytes); return r; };
     w.hdr = reinterpret_cast<WsHeader*>(p); p += sizeof(WsHeader);
-    w.logits = reinterpret_cast<float*>(take(sizeof(float) * (size_t)T * d.E));
+    w.logits = reinterpret_cast<float*>(take(sizeof(float) * (size_t)T * d.E * router_splits(d.H, T, d.E)));
     w.gate = reinterpret_cast<float*>(take(sizeof(float) * (size_t)T));
     w.ids = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * Tk));
     w.w = reinterpret_cast<float*>(take(sizeof(float) * Tk));
@@ -397,7 +420,9 @@ PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T) {
     return w;
 }
 
-int prefill_launch_count(const moe_layer_desc& d) { return d.Is > 0 ? 9 : 8; }
+int prefill_launch_count(const moe_layer_desc& d, int T) {
+    return (d.Is > 0 ? 9 : 8) + (router_splits(d.H, T, d.E) > 1 ? 1 : 0);
+}
 
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
@@ -410,9 +435,16 @@ cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T
     // 1. router logits (+ the shared gate pre-activation)
     {
         const dim3 grid((T + kBM - 1) / kBM, (E + kBN - 1) / kBN);
-        router_gemm_kernel<<<grid, kGThreads, 4 * kBM * kLds * sizeof(uint16_t), s>>>(x, T, H, d.router_w, E,
-                                                                                      ws.logits);
+        const int splits = router_splits(H, T, E);
+        const dim3 gridk(grid.x, grid.y, splits);
+        router_gemm_kernel<<<gridk, kGThreads, 4 * kBM * kLds * sizeof(uint16_t), s>>>(x, T, H, d.router_w, E,
+                                                                                       H / splits, ws.logits);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (splits > 1) {
+            const int n4 = T * E / 4;
+            router_sum_kernel<<<(n4 + 255) / 256, 256, 0, s>>>(ws.logits, n4, splits, (size_t)T * E / 4);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
         if (d.Is > 0) {
             gate_dot_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, d.sh_gate_w, ws.gate);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
