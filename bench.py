@@ -424,12 +424,52 @@ def main():
     torch.cuda.synchronize()
     e2e_us = 1e3 * e0.elapsed_time(e1) / Ke
 
+    # batched decode: 8 and 64 tokens per call through the same rotating layers (the
+    # multi-token kernels), graph-replayed like the single-token steps
+    batched = []
+    for Tb in (8, 64):
+        xb = [wl.activations(100 + i, Tb, layers[0].H, device=device) for i in range(n_inst)]
+        wsb = nv.Workspace(nv.moe_layer_workspace_size(layers[0], Tb), device=device)
+        yb = [torch.empty(Tb, layers[0].H, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
+        idsb = []
+        for i in range(n_inst):
+            _, ids_i, _ = nv.moe_layer_forward(layers[i], xb[i], ws=wsb, want_route=True, desc=descs[i])
+            idsb.append(ids_i.cpu().numpy().ravel())
+        bytes_b = sum(step_bytes(layers[i], idsb[i], T=Tb) for i in range(n_inst)) / n_inst
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            for i in range(n_inst):
+                nv.moe_layer_forward(layers[i], xb[i], ws=wsb, y=yb[i], desc=descs[i])
+            torch.cuda.synchronize()
+            with torch.cuda.graph(gb, stream=cap):
+                for i in range(n_inst):
+                    nv.moe_layer_forward(layers[i], xb[i], ws=wsb, y=yb[i], desc=descs[i])
+        torch.cuda.synchronize()
+        for _ in range(3):
+            gb.replay()
+        torch.cuda.synchronize()
+        rb = max(1, 200 // n_inst)
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(rb):
+            gb.replay()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        us_call = 1e3 * b0.elapsed_time(b1) / (rb * n_inst)
+        gbs = bytes_b / (us_call * 1e-6) / 1e9
+        batched.append({"tokens": Tb, "us_per_call": us_call, "us_per_token": us_call / Tb,
+                        "bytes_per_call": bytes_b, "achieved_gbs": gbs})
+        del wsb
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
     peak, peak_kind = measured_peaks()
+    for b in batched:
+        b["frac_of_hbm_peak"] = b["achieved_gbs"] / peak if peak else None
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         us, n, tot = cpu_oracle_sample(args.cpu_seconds)
@@ -457,6 +497,7 @@ def main():
         "gpu_launches": launches_per_step * K,
         "timing": {"mode": "CUDA graph replay of %d-step passes" % n_inst,
                    "stream_launch_us_per_token": stream_us},
+        "batched_decode": batched,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
