@@ -1,0 +1,480 @@
+// MoE layer, multi-token decode (1..64 tokens per call, E4M3 block scales): router
+// GEMV, fused route, grouped gate/up + SwiGLU and grouped down on the warp-level
+// tensor cores, then the routing-weighted combine.
+//
+// Sources (page title, section):
+//  - lynn-engine tutorials index, row 06 "MoE router" (softmax over all experts ->
+//    top-k -> renormalise; sigmoid-gated shared expert).
+//  - lynn-engine README, P28 note (gate/up + SiLU over the active experts only,
+//    [top_k, I] intermediate), P29 note (down + weighted sum -> [H]), P46/P48 notes
+//    (no float atomics in the combine: every output element is summed by one
+//    thread in a fixed order).
+//
+// Each routed expert with n entries, and the shared expert (whose entries are the T
+// tokens), is a small GEMM: weight rows times up to 16 entries per pass. The weight
+// rows sit on the M side of mma.sync m16n8k16 (bf16 in, fp32 accumulate), the
+// entries on its N side (one or two n8 blocks). The NVFP4 codes go from HBM into
+// registers and are expanded there, exactly, into the A fragments: no shared-memory
+// round trip and no bf16 copy of a weight. The entries' bf16 rows (x for gate/up,
+// h for down) are staged once per CTA in shared memory and read as B fragments.
+//
+// K order. A contraction may visit K in any order as long as both operands use the
+// same one. In 256-element chunk j, the lanes of quad position q (lane % 4) own the
+// 64 elements [256j + 64q, 256j + 64q + 64): 32 code bytes (two 16-byte loads per
+// weight row) and 4 block scales (one 32-bit load). MMA step s (0..15) of the chunk
+// takes elements 256j + 64q + 4s + {0, 1} as fragment k positions {2q, 2q+1} and
+// + {2, 3} as {2q+8, 2q+9}, in A and in B alike; each lane's four elements of a
+// step are one 16-element scale block.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPass = 16;          // entries per pass: two n8 MMA blocks
+constexpr int kGuPairs = 64;       // gate/up row pairs per CTA item (8 per warp)
+constexpr int kDnRows = 128;       // down output rows per CTA item (16 per warp)
+constexpr int kRouterTok = 16;     // tokens per router CTA
+constexpr int kMaxDim = 4096;      // H, I, Is bound of this path (shared-memory staging)
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Staged row r, 8-byte unit u (four bf16) lives at unit u ^ (((u >> 2) & 12) | (r & 3)).
+// In one MMA step the 16 lanes of a half-warp (rows r & 3 = g & 3, quads q) read
+// units whose low four bits are s ^ (4q | (g & 3)): 16 distinct bank pairs.
+__device__ __forceinline__ uint32_t swz(uint32_t u, uint32_t r) { return u ^ (((u >> 2) & 12u) | (r & 3u)); }
+
+// Copy n bf16 rows of K elements (row r from row_ptr(r)) into the swizzled layout.
+template <class RowPtr>
+__device__ __forceinline__ void stage_rows(uint8_t* sm, int n, int K, RowPtr row_ptr) {
+    const int per_row = K >> 3;   // 16-byte granules = two units
+    for (int i = threadIdx.x; i < n * per_row; i += kThreads) {
+        const int r = i / per_row, v = i - r * per_row;
+        const uint4 val = *reinterpret_cast<const uint4*>(row_ptr(r) + 8 * (size_t)v);
+        uint2* dst = reinterpret_cast<uint2*>(sm + (size_t)r * K * 2);
+        dst[swz(2 * v, r)] = make_uint2(val.x, val.y);
+        dst[swz(2 * v + 1, r)] = make_uint2(val.z, val.w);
+    }
+}
+
+// One weight row's share of a chunk for one lane: 32 code bytes and 4 E4M3 scales.
+struct WChunk {
+    uint4 lo, hi;
+    uint32_t sc;
+};
+
+__device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t* scl, int j) {
+    WChunk c;
+    c.lo = ld_stream_v4(codes + 128 * j);
+    c.hi = ld_stream_v4(codes + 128 * j + 16);
+    c.sc = ld_stream_u32(scl + 16 * j);
+    return c;
+}
+
+// 32-bit word of the chunk holding the code bytes of MMA step s (bytes 2s, 2s+1).
+__device__ __forceinline__ uint32_t step_word(const WChunk& c, int s) {
+    const uint4& v = s < 8 ? c.lo : c.hi;
+    const int w = (s >> 1) & 3;
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+// The 16 MMA steps of one chunk: A rows (r0: fragment rows 0-7, r1: rows 8-15),
+// B from nb staged n8 blocks (row g and g + 8 of the stage).
+template <int NB>
+__device__ __forceinline__ void chunk_mma(float (&acc)[2][4], const WChunk& c0, const WChunk& c1,
+                                          const uint8_t* brow0, const uint8_t* brow1, uint32_t ubase,
+                                          uint32_t xmask) {
+    uint32_t s0[4], s1[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        s0[b] = e4m3_to_bf16x2_x2p112((c0.sc >> (8 * b)) & 0xFFu);
+        s1[b] = e4m3_to_bf16x2_x2p112((c1.sc >> (8 * b)) & 0xFFu);
+    }
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        const uint32_t w0 = step_word(c0, s) >> (16 * (s & 1));
+        const uint32_t w1 = step_word(c1, s) >> (16 * (s & 1));
+        const uint32_t a0 = e2m1x2_to_bf16x2_scaled(w0, s0[s >> 2]);
+        const uint32_t a1 = e2m1x2_to_bf16x2_scaled(w1, s1[s >> 2]);
+        const uint32_t a2 = e2m1x2_to_bf16x2_scaled(w0 >> 8, s0[s >> 2]);
+        const uint32_t a3 = e2m1x2_to_bf16x2_scaled(w1 >> 8, s1[s >> 2]);
+        const uint32_t off = 8u * (ubase + ((uint32_t)s ^ xmask));
+        const uint2 b0 = *reinterpret_cast<const uint2*>(brow0 + off);
+        mma_16816(acc[0], a0, a1, a2, a3, b0.x, b0.y);
+        if (NB == 2) {
+            const uint2 b1 = *reinterpret_cast<const uint2*>(brow1 + off);
+            mma_16816(acc[1], a0, a1, a2, a3, b1.x, b1.y);
+        }
+    }
+}
+
+// K loop over nchunk chunks with the next chunk's loads in flight during the MMAs.
+template <int NB>
+__device__ __forceinline__ void k_loop(float (&acc)[2][4], const uint8_t* codes0, const uint8_t* scl0,
+                                       const uint8_t* codes1, const uint8_t* scl1, int nchunk,
+                                       const uint8_t* brow0, const uint8_t* brow1, uint32_t q,
+                                       uint32_t xmask, WChunk c0, WChunk c1) {
+    for (int j = 0; j < nchunk; ++j) {
+        WChunk n0 = c0, n1 = c1;
+        if (j + 1 < nchunk) {
+            n0 = load_chunk(codes0, scl0, j + 1);
+            n1 = load_chunk(codes1, scl1, j + 1);
+        }
+        chunk_mma<NB>(acc, c0, c1, brow0, brow1, 64u * j + 16u * q, xmask);
+        c0 = n0;
+        c1 = n1;
+    }
+}
+
+// ------------------------------------------------------------------ router
+// logits[t, e] = x[t] . Wg[e] (e < E); gate_logit[t] = x[t] . gs (row E). CTA =
+// 8 rows (a warp each) x 16 tokens; a lane holds its 16-byte chunks of the row as
+// fp32 and reads the tokens' chunks from shared memory (consecutive lanes,
+// consecutive 16 bytes: conflict-free).
+__global__ void __launch_bounds__(kThreads)
+router_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restrict__ gs,
+                 const uint16_t* __restrict__ x, int T, int E, int H, float* __restrict__ logits,
+                 float* __restrict__ gate_logit) {
+    extern __shared__ uint4 xs4[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = H >> 3;
+    const int rows = E + (gs ? 1 : 0);
+    const int r = blockIdx.x * kWarps + warp;
+    const int t0 = blockIdx.y * kRouterTok;
+    const int tc = min(kRouterTok, T - t0);
+    for (int i = threadIdx.x; i < tc * nch; i += kThreads)
+        xs4[i] = *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + 8 * (size_t)i);
+    __syncthreads();
+    if (r >= rows) return;
+    const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
+    float acc[kRouterTok];
+#pragma unroll
+    for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
+    for (int g0 = 0; g0 < nch; g0 += 256) {          // 8 chunks per lane per group
+        float wf[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = g0 + lane + 32 * i;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (c < nch) v = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
+            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                wf[i][2 * p] = bf16lo(ww[p]);
+                wf[i][2 * p + 1] = bf16hi(ww[p]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) {
+            if (t < tc) {
+                float a = acc[t];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = g0 + lane + 32 * i;
+                    if (c < nch) {
+                        const uint4 xv = xs4[t * nch + c];
+                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
+                            a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
+                        }
+                    }
+                }
+                acc[t] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTok; ++t) {
+        if (t < tc) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) {
+                if (r < E) logits[(size_t)(t0 + t) * E + r] = v;
+                else gate_logit[t0 + t] = v;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ gate/up
+// Item = (slot pass, block of 64 row pairs). Routed passes come from the pass map
+// (active slot a, entries [16 pi, 16 pi + 16) of expert a's list); the shared
+// expert's pass pi is tokens [16 pi, 16 pi + 16). Warp w takes gate rows
+// i0 + 8w + g as fragment rows 0-7 and the matching up rows as rows 8-15, so lane
+// (g, q) ends with gate and up of row i0 + 8w + g for entries 2q, 2q+1 of each n8
+// block: h = silu(ts_g * gate) * (ts_u * up), written as bf16.
+__global__ void __launch_bounds__(kThreads, 3)
+gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
+                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ token_list,
+                 const int32_t* __restrict__ active, const int32_t* __restrict__ pass_map,
+                 uint16_t* __restrict__ h, uint16_t* __restrict__ hs) {
+    extern __shared__ __align__(16) uint8_t stage[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t g = lane >> 2, q = lane & 3;
+    const int H = d.H, k = d.k;
+    const int rb_r = d.I / kGuPairs, rb_s = d.Is / kGuPairs;
+    const int items_r = pass_map[0] * rb_r;
+    const int items = items_r + (T + kPass - 1) / kPass * rb_s;
+    const int nchunk = H >> 8;
+    const uint32_t xmask = 4u * q | (g & 3u);
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const uint8_t* codes;
+        const uint8_t* scl;
+        const int32_t* list;   // routed: the pass's entries; shared: none (tokens first + r)
+        float tsg, tsu;
+        int Irows, i0, n, first;
+        uint16_t* out;
+        if (item < items_r) {
+            const int p = item / rb_r;
+            const int pm = pass_map[1 + p];
+            const int e = active[1 + (pm >> 8)];
+            const int beg = offsets[e] + kPass * (pm & 255);
+            n = min(kPass, offsets[e + 1] - beg);
+            list = token_list + beg;
+            first = 0;
+            i0 = (item - p * rb_r) * kGuPairs;
+            Irows = d.I;
+            codes = d.gu_packed + (size_t)e * 2 * d.I * (H / 2);
+            scl = static_cast<const uint8_t*>(d.gu_scales) + (size_t)e * 2 * d.I * (H / 16);
+            tsg = __ldg(d.gu_tscale + 2 * e);
+            tsu = __ldg(d.gu_tscale + 2 * e + 1);
+            out = h;
+        } else {
+            const int it = item - items_r;
+            const int pi = it / rb_s;
+            first = kPass * pi;
+            n = min(kPass, T - first);
+            list = nullptr;
+            i0 = (it - pi * rb_s) * kGuPairs;
+            Irows = d.Is;
+            codes = d.sh_gu_packed;
+            scl = static_cast<const uint8_t*>(d.sh_gu_scales);
+            tsg = __ldg(d.sh_gu_tscale);
+            tsu = __ldg(d.sh_gu_tscale + 1);
+            out = hs;
+        }
+        const int i = i0 + 8 * warp + (int)g;
+        const uint8_t* cg = codes + (size_t)i * (H / 2) + 32 * q;
+        const uint8_t* cu = codes + (size_t)(Irows + i) * (H / 2) + 32 * q;
+        const uint8_t* sg = scl + (size_t)i * (H / 16) + 4 * q;
+        const uint8_t* su = scl + (size_t)(Irows + i) * (H / 16) + 4 * q;
+        const WChunk c0 = load_chunk(cg, sg, 0), c1 = load_chunk(cu, su, 0);
+        __syncthreads();   // the previous item's MMAs are done with the stage
+        stage_rows(stage, n, H, [&](int r) { return x + (size_t)(list ? list[r] / k : first + r) * H; });
+        __syncthreads();
+        float acc[2][4] = {};
+        const uint8_t* b0 = stage + (size_t)g * H * 2;
+        const uint8_t* b1 = stage + (size_t)(g + 8) * H * 2;
+        if (n > 8) k_loop<2>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1);
+        else k_loop<1>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1);
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = 8 * nb + 2 * (int)q + c;
+                if (r < n) {
+                    const float gv = acc[nb][c] * tsg, uv = acc[nb][2 + c] * tsu;
+                    const size_t row = list ? (size_t)list[r] : (size_t)(first + r);
+                    out[row * Irows + i] = f32_to_bf16(silu_f32(gv) * uv);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ down
+// Item = (slot pass, block of 128 output rows). Warp w takes rows
+// nr = 128 rb + 16w + g (fragment rows 0-7) and nr + 8 (rows 8-15) over K = I
+// (Is for the shared expert). Output rows, fp32, one writer each:
+//   P[entry, n] = w_entry * ts_e * (D_e[n] . h_entry)          (routed)
+//   Ps[t, n]    = sigmoid(gate_t) * ts_s * (Ds[n] . hs_t)       (shared)
+__global__ void __launch_bounds__(kThreads, 3)
+down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
+               const int32_t* __restrict__ token_list, const int32_t* __restrict__ active,
+               const int32_t* __restrict__ pass_map, const float* __restrict__ wts,
+               const float* __restrict__ gate_logit, const uint16_t* __restrict__ h,
+               const uint16_t* __restrict__ hs, float* __restrict__ P, float* __restrict__ Ps) {
+    extern __shared__ __align__(16) uint8_t stage[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t g = lane >> 2, q = lane & 3;
+    const int H = d.H;
+    const int rb_n = H / kDnRows;
+    const int items_r = pass_map[0] * rb_n;
+    const int items = items_r + (d.Is > 0 ? (T + kPass - 1) / kPass * rb_n : 0);
+    const uint32_t xmask = 4u * q | (g & 3u);
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const uint8_t* codes;
+        const uint8_t* scl;
+        const int32_t* list;
+        const uint16_t* src;
+        float ts;
+        int K, n, first, rb;
+        if (item < items_r) {
+            const int p = item / rb_n;
+            const int pm = pass_map[1 + p];
+            const int e = active[1 + (pm >> 8)];
+            const int beg = offsets[e] + kPass * (pm & 255);
+            n = min(kPass, offsets[e + 1] - beg);
+            list = token_list + beg;
+            first = 0;
+            rb = item - p * rb_n;
+            K = d.I;
+            codes = d.dn_packed + (size_t)e * H * (K / 2);
+            scl = static_cast<const uint8_t*>(d.dn_scales) + (size_t)e * H * (K / 16);
+            ts = __ldg(d.dn_tscale + e);
+            src = h;
+        } else {
+            const int it = item - items_r;
+            const int pi = it / rb_n;
+            first = kPass * pi;
+            n = min(kPass, T - first);
+            list = nullptr;
+            rb = it - pi * rb_n;
+            K = d.Is;
+            codes = d.sh_dn_packed;
+            scl = static_cast<const uint8_t*>(d.sh_dn_scales);
+            ts = __ldg(d.sh_dn_tscale);
+            src = hs;
+        }
+        const int nr = rb * kDnRows + 16 * warp + (int)g;
+        const uint8_t* c0p = codes + (size_t)nr * (K / 2) + 32 * q;
+        const uint8_t* c1p = codes + (size_t)(nr + 8) * (K / 2) + 32 * q;
+        const uint8_t* s0p = scl + (size_t)nr * (K / 16) + 4 * q;
+        const uint8_t* s1p = scl + (size_t)(nr + 8) * (K / 16) + 4 * q;
+        const WChunk c0 = load_chunk(c0p, s0p, 0), c1 = load_chunk(c1p, s1p, 0);
+        __syncthreads();
+        stage_rows(stage, n, K, [&](int r) { return src + (size_t)(list ? list[r] : first + r) * K; });
+        __syncthreads();
+        float acc[2][4] = {};
+        const uint8_t* b0 = stage + (size_t)g * K * 2;
+        const uint8_t* b1 = stage + (size_t)(g + 8) * K * 2;
+        if (n > 8) k_loop<2>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1);
+        else k_loop<1>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1);
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = 8 * nb + 2 * (int)q + c;
+                if (r < n) {
+                    if (list) {
+                        const int en = list[r];
+                        const float f = wts[en] * ts;
+                        P[(size_t)en * H + nr] = acc[nb][c] * f;
+                        P[(size_t)en * H + nr + 8] = acc[nb][2 + c] * f;
+                    } else {
+                        const int t = first + r;
+                        const float f = sigmoid_f32(gate_logit[t]) * ts;
+                        Ps[(size_t)t * H + nr] = acc[nb][c] * f;
+                        Ps[(size_t)t * H + nr + 8] = acc[nb][2 + c] * f;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ combine
+// y[t, n] = bf16( sum_j P[t*k + j, n]  (j = 0..k-1)  + Ps[t, n] ), that order.
+__global__ void __launch_bounds__(kThreads)
+combine_mt_kernel(const float* __restrict__ P, const float* __restrict__ Ps, int T, int H, int k,
+                  uint16_t* __restrict__ y) {
+    const int q4 = H >> 2;
+    const int i = blockIdx.x * kThreads + threadIdx.x;
+    if (i >= T * q4) return;
+    const int t = i / q4, c = i - t * q4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(P + (size_t)(t * k + j) * H + 4 * c);
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    if (Ps) {
+        const float4 v = *reinterpret_cast<const float4*>(Ps + (size_t)t * H + 4 * c);
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16(a.x) | ((uint32_t)f32_to_bf16(a.y) << 16);
+    o.y = (uint32_t)f32_to_bf16(a.z) | ((uint32_t)f32_to_bf16(a.w) << 16);
+    *reinterpret_cast<uint2*>(y + (size_t)t * H + 4 * c) = o;
+}
+
+int resident_ctas(const void* fn, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess || n < 1) n = 1;
+    return n;
+}
+
+}  // namespace
+
+bool decode_mma_supported(const moe_layer_desc& d, int T) {
+    return d.kind == NVFP4_SCALE_E4M3 && T >= 1 && T <= NVFP4_DECODE_MAX_TOKENS && d.H % 256 == 0 &&
+           d.I % 256 == 0 && d.Is % 256 == 0 && d.H <= kMaxDim && d.I <= kMaxDim && d.Is <= kMaxDim;
+}
+
+cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
+                                  int32_t* ids_out, float* w_out, const LayerWs& ws, const DeviceInfo& dev,
+                                  cudaStream_t s) {
+    cudaError_t err;
+    const bool shared = d.Is > 0;
+    const int passes_shared = (T + kPass - 1) / kPass;
+    const int passes_routed_ub = (d.E < T * d.k ? d.E : T * d.k) + T * d.k / kPass;
+    uint16_t* h = reinterpret_cast<uint16_t*>(ws.h);
+    uint16_t* hs = reinterpret_cast<uint16_t*>(ws.hs);
+    float* P = ws.part;
+    float* Ps = shared ? ws.part + (size_t)T * d.k * d.H : nullptr;
+    {   // 1. router GEMV (+ the shared gate's pre-activation)
+        const int rows = d.E + (shared ? 1 : 0);
+        const dim3 grid((rows + kWarps - 1) / kWarps, (T + kRouterTok - 1) / kRouterTok);
+        const size_t smem = (size_t)(T < kRouterTok ? T : kRouterTok) * d.H * 2;
+        err = cudaFuncSetAttribute(router_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        router_mt_kernel<<<grid, kThreads, smem, s>>>(d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E,
+                                                      d.H, ws.logits, ws.gate_logit);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    // 2. top-k, lists, active experts and the pass map (one block)
+    if ((err = launch_route_mt(ws.logits, T, d.E, d.k, ws.ids, ws.w, ids_out, w_out, ws.offsets,
+                               ws.token_list, ws.active, ws.pass_map, s)) != cudaSuccess)
+        return err;
+    {   // 3. gate/up + SwiGLU
+        const size_t smem = (size_t)kPass * d.H * 2;
+        err = cudaFuncSetAttribute(gateup_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        const long items_ub = (long)passes_routed_ub * (d.I / kGuPairs) +
+                              (shared ? (long)passes_shared * (d.Is / kGuPairs) : 0);
+        const long cap = (long)dev.num_sms * resident_ctas((const void*)gateup_mt_kernel, smem);
+        const int grid = (int)(items_ub < cap ? items_ub : cap);
+        gateup_mt_kernel<<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
+                                                      ws.pass_map, h, hs);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {   // 4. down, weighted rows
+        const int K = d.I > d.Is ? d.I : d.Is;
+        const size_t smem = (size_t)kPass * K * 2;
+        err = cudaFuncSetAttribute(down_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        const long items_ub = (long)(passes_routed_ub + (shared ? passes_shared : 0)) * (d.H / kDnRows);
+        const long cap = (long)dev.num_sms * resident_ctas((const void*)down_mt_kernel, smem);
+        const int grid = (int)(items_ub < cap ? items_ub : cap);
+        down_mt_kernel<<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active, ws.pass_map,
+                                                    ws.w, ws.gate_logit, h, hs, P, Ps);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    {   // 5. combine
+        const int n = T * (d.H / 4);
+        combine_mt_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, s>>>(P, Ps, T, d.H, d.k, y);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace nvfp4

@@ -25,6 +25,10 @@ cudaError_t launch_route_lists(const int32_t* ids, int total, int E, int32_t* of
                                int32_t* token_list, int32_t* active, cudaStream_t s);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          int32_t* offsets, int32_t* token_list, cudaStream_t s);
+// Fused top-k + lists + active list + pass map for T*k <= 512 (one block).
+cudaError_t launch_route_mt(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                            int32_t* ids_out, float* w_out, int32_t* offsets, int32_t* token_list,
+                            int32_t* active, int32_t* pass_map, cudaStream_t s);
 
 // Workspace of one layer call (device scratch carved from the caller's buffer).
 struct LayerWs {
@@ -39,6 +43,8 @@ struct LayerWs {
     float* h;             // [T * k, I] routed SwiGLU intermediates (entry-major)
     float* hs;            // [T, Is]    shared intermediates
     unsigned long long* words;  // [E + 2 + k*I + Is] (launch tag, value) words of the one-launch kernel
+    int32_t* pass_map;    // [E + T*k + 2]  pass_map[0] = P, then (active slot << 8) | pass
+    float* part;          // [T*k + T, H]  weighted routed rows, then the shared rows
     size_t bytes;
 };
 
@@ -48,6 +54,12 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T);
 cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                               int32_t* ids_out, float* w_out, const LayerWs& ws,
                               const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
+
+// Multi-token decode on mma.sync (E4M3 scales, H, I, Is multiples of 256, <= 4096).
+bool decode_mma_supported(const moe_layer_desc& d, int T);
+cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
+                                  int32_t* ids_out, float* w_out, const LayerWs& ws, const DeviceInfo& dev,
+                                  cudaStream_t s);
 
 // One-launch single-token decode (persistent grid, two bounded grid barriers).
 bool fused_decode_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev);

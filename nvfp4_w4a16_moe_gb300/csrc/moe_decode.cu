@@ -355,6 +355,8 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T) {
     b += align256(sizeof(float) * Tk * d.I);
     b += align256(sizeof(float) * (size_t)T * d.Is);
     b += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
+    b += align256(sizeof(int32_t) * (Tk + d.E + 2));
+    b += align256(sizeof(float) * (Tk + T) * d.H);
     return b;
 }
 
@@ -374,6 +376,8 @@ LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T) {
     w.hs = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (size_t)T * d.Is);
     w.words = reinterpret_cast<unsigned long long*>(p);
     p += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
+    w.pass_map = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * (Tk + d.E + 2));
+    w.part = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (Tk + T) * d.H);
     w.bytes = (size_t)(p - static_cast<char*>(base));
     return w;
 }
@@ -432,6 +436,7 @@ cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T,
                               int32_t* ids_out, float* w_out, const LayerWs& ws,
                               const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s) {
     (void)wait_limit;
+    if (decode_mma_supported(d, T)) return launch_moe_decode_mma(d, x, T, y, ids_out, w_out, ws, dev, s);
     if (d.kind == NVFP4_SCALE_E4M3) return decode_impl<NVFP4_SCALE_E4M3>(d, x, T, y, ids_out, w_out, ws, dev, s);
     return decode_impl<NVFP4_SCALE_FP16>(d, x, T, y, ids_out, w_out, ws, dev, s);
 }
