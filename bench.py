@@ -39,9 +39,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seeds", type=int, default=N_SEEDS, help="layer instances to rotate over")
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched"],
                     help="decode: the single-token layer (default, the headline); prefill: one "
-                         "4096-token layer call with the skewed router")
+                         "4096-token layer call with the skewed router; batched: one --tokens-token "
+                         "decode call per step")
+    ap.add_argument("--tokens", type=int, default=64, help="tokens per call of --workload batched (1..64)")
     return ap.parse_args()
 
 
@@ -302,6 +304,76 @@ def run_prefill(args, nv, wl, device):
     return 0
 
 
+def run_batched(args, nv, wl, device):
+    """One decode call of --tokens tokens per step through --seeds rotating layer
+    instances (the multi-token kernels), CUDA-graph replayed in passes over the
+    instances; bytes per call are the distinct active experts' weights plus the
+    shared expert, the router and the activations."""
+    Tb = args.tokens
+    n_inst = max(1, args.seeds)
+    layers, _ = build_layers(nv, wl, device, n_inst)
+    descs = [l.desc() for l in layers]
+    xb = [wl.activations(100 + i, Tb, layers[0].H, device=device) for i in range(n_inst)]
+    yb = [torch.empty(Tb, layers[0].H, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
+    ws = nv.Workspace(nv.moe_layer_workspace_size(layers[0], Tb), device=device)
+    ids = []
+    for i in range(n_inst):
+        _, ids_i, _ = nv.moe_layer_forward(layers[i], xb[i], ws=ws, want_route=True, desc=descs[i])
+        ids.append(ids_i.cpu().numpy().ravel())
+    bytes_call = sum(step_bytes(layers[i], ids[i], T=Tb) for i in range(n_inst)) / n_inst
+    stream = torch.cuda.current_stream()
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        for i in range(n_inst):
+            nv.moe_layer_forward(layers[i], xb[i], ws=ws, y=yb[i], desc=descs[i])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(n_inst):
+                nv.moe_layer_forward(layers[i], xb[i], ws=ws, y=yb[i], desc=descs[i])
+    torch.cuda.synchronize()
+    W = max(3, args.warmup)
+    for _ in range(-(-W // n_inst)):
+        g.replay()
+    torch.cuda.synchronize()
+    passes = max(1, -(-max(1, args.steps) // n_inst))
+    K = passes * n_inst
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index or 0) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(passes):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    us = 1e3 * ev0.elapsed_time(ev1) / K
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": "NVFP4 MoE-layer decode, %d tokens per call: us/token and achieved HBM GB/s" % Tb,
+        "value": us / Tb, "unit": "us/token", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": us * 1e-3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-act/nvfp4-weight, bf16 MMA, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
+        "config": {"workload": "qwen3.6-35b-a3b-shaped MoE layer decode, T=%d tokens per call, H=2048 E=256 "
+                               "top-8 I=512 shared Is=512, NVFP4 E4M3 per-16 scales, %d rotating instances"
+                               % (Tb, n_inst), "tokens_per_step": Tb},
+        "us_per_call": us, "achieved_gbs": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak if peak else None, "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": bytes_call,
+                     "kernel": "whole call (router, route, gate/up, down, combine): algorithmic bytes / call time"},
+        "gpu_launches": nv.launches_per_layer_call(Tb, layers[0].H) * K,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -321,6 +393,10 @@ def main():
         if world > 1 and rank != 0:
             return 0
         return run_prefill(args, nv, wl, device)
+    if args.workload == "batched":
+        if world > 1 and rank != 0:
+            return 0
+        return run_batched(args, nv, wl, device)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)

@@ -25,19 +25,25 @@ SCALE_E4M3 = 0
 SCALE_FP16 = 1
 
 
-def launches_per_layer_call(T: int, H: int = 2048, kind: int = 0, shared: bool = True, E: int = 256) -> int:
+def launches_per_layer_call(T: int, H: int = 2048, kind: int = 0, shared: bool = True, E: int = 256,
+                            I: int = 512, Is: int = 512) -> int:
     """Kernel launches one moe_layer_forward call enqueues (routing outputs not requested):
-    one for the single-token fused kernel, five for the multi-token decode path (per
-    64-token chunk for FP16-scaled layers above 64 tokens), and for the prefill path
-    router (and the sum of its K-split partials), gate, top-k, three list passes,
-    gate/up, down and combine (no gate launch without a shared expert)."""
+    one for the single-token fused kernel; four for the tensor-core multi-token decode
+    path (router + route, gate/up, down, combine; E4M3 scales, H, I, Is multiples of
+    256 and at most 4096); five for the other multi-token shapes (router, top-k, lists,
+    gate/up, down), per 64-token chunk for FP16-scaled layers above 64 tokens; and for
+    the prefill path router (and the sum of its K-split partials), gate, top-k, three
+    list passes, gate/up, down and combine (no gate launch without a shared expert)."""
     if T == 1 and H % 256 == 0 and H <= 2048:
         return 1
+    mma = (kind == 0 and H % 256 == 0 and I % 256 == 0 and Is % 256 == 0 and
+           H <= 4096 and I <= 4096 and Is <= 4096)
     if T <= 64:
-        return 5
+        return 4 if mma else 5
     if kind == 0:
         return (9 if shared else 8) + (1 if (H // 32) % 2 == 0 and (T * E) % 4 == 0 else 0)
     return 5 * ((T + 63) // 64)
+
 
 STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pointer not 16-byte aligned",

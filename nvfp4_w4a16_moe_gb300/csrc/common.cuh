@@ -14,13 +14,16 @@ namespace nvfp4 {
 // ---------------------------------------------------------------- workspace
 // Every workspace starts with this header. `status` holds an nvfp4_status the
 // device recorded; `barrier` counts grid-barrier arrivals monotonically across
-// launches (one 64-bit counter never wraps in practice).
+// launches (one 64-bit counter never wraps in practice); `route_tickets` count
+// the router blocks of one multi-token call that are done (per 16-token block,
+// then over token blocks) and are reset to 0 by the block that finishes last.
 struct alignas(256) WsHeader {
     uint32_t status;
     uint32_t pad0;
     unsigned long long barrier;
     unsigned int amax_bits;      // nvfp4_pack: max |w| as fp32 bits
-    unsigned int pad1[59];
+    unsigned int route_tickets[5];
+    unsigned int pad1[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -27,6 +27,7 @@
 // step are one 16-element scale block.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "route_mt.cuh"
 
 namespace nvfp4 {
 
@@ -80,15 +81,33 @@ __device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t
     return c;
 }
 
-// 32-bit word of the chunk holding the code bytes of MMA step s (bytes 2s, 2s+1).
-__device__ __forceinline__ uint32_t step_word(const WChunk& c, int s) {
-    const uint4& v = s < 8 ? c.lo : c.hi;
-    const int w = (s >> 1) & 3;
+// Four E2M1 code bytes (one 32-bit word, two MMA steps of one weight row) ->
+// four bf16x2 of code * scale. The word is unpacked into byte registers for cvt
+// (no shifts); the f16 -> bf16 re-reading (magnitude >> 3, sign kept, see
+// e2m1x2_to_bf16x2_scaled) takes its shift as a 32x32 -> high-32 multiply by
+// 2^29, which runs on the FMA pipe instead of the integer ALU.
+__device__ __forceinline__ void expand_word(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+    uint32_t h[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t m = __umulhi(h[b] & 0x7FFF7FFFu, 1u << 29) | (h[b] & 0x80008000u);
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(m), "r"(s2));
+    }
+}
+
+__device__ __forceinline__ uint32_t word_of(const WChunk& c, int wi) {
+    const uint4& v = wi < 4 ? c.lo : c.hi;
+    const int w = wi & 3;
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
-// The 16 MMA steps of one chunk: A rows (r0: fragment rows 0-7, r1: rows 8-15),
-// B from nb staged n8 blocks (row g and g + 8 of the stage).
+// The 16 MMA steps of one chunk: A rows (c0: fragment rows 0-7, c1: rows 8-15),
+// B from NB staged n8 blocks (row g and g + 8 of the stage). Code word wi holds
+// steps 2wi (bytes 0, 1) and 2wi + 1 (bytes 2, 3), both in scale block wi / 2.
 template <int NB>
 __device__ __forceinline__ void chunk_mma(float (&acc)[2][4], const WChunk& c0, const WChunk& c1,
                                           const uint8_t* brow0, const uint8_t* brow1, uint32_t ubase,
@@ -100,19 +119,20 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[2][4], const WChunk& c0, 
         s1[b] = e4m3_to_bf16x2_x2p112((c1.sc >> (8 * b)) & 0xFFu);
     }
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        const uint32_t w0 = step_word(c0, s) >> (16 * (s & 1));
-        const uint32_t w1 = step_word(c1, s) >> (16 * (s & 1));
-        const uint32_t a0 = e2m1x2_to_bf16x2_scaled(w0, s0[s >> 2]);
-        const uint32_t a1 = e2m1x2_to_bf16x2_scaled(w1, s1[s >> 2]);
-        const uint32_t a2 = e2m1x2_to_bf16x2_scaled(w0 >> 8, s0[s >> 2]);
-        const uint32_t a3 = e2m1x2_to_bf16x2_scaled(w1 >> 8, s1[s >> 2]);
-        const uint32_t off = 8u * (ubase + ((uint32_t)s ^ xmask));
-        const uint2 b0 = *reinterpret_cast<const uint2*>(brow0 + off);
-        mma_16816(acc[0], a0, a1, a2, a3, b0.x, b0.y);
-        if (NB == 2) {
-            const uint2 b1 = *reinterpret_cast<const uint2*>(brow1 + off);
-            mma_16816(acc[1], a0, a1, a2, a3, b1.x, b1.y);
+    for (int wi = 0; wi < 8; ++wi) {
+        uint32_t a[4], u[4];
+        expand_word(word_of(c0, wi), s0[wi >> 1], a);
+        expand_word(word_of(c1, wi), s1[wi >> 1], u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int s = 2 * wi + h;
+            const uint32_t off = 8u * (ubase + ((uint32_t)s ^ xmask));
+            const uint2 b0 = *reinterpret_cast<const uint2*>(brow0 + off);
+            mma_16816(acc[0], a[2 * h], u[2 * h], a[2 * h + 1], u[2 * h + 1], b0.x, b0.y);
+            if (NB == 2) {
+                const uint2 b1 = *reinterpret_cast<const uint2*>(brow1 + off);
+                mma_16816(acc[1], a[2 * h], u[2 * h], a[2 * h + 1], u[2 * h + 1], b1.x, b1.y);
+            }
         }
     }
 }
@@ -135,16 +155,23 @@ __device__ __forceinline__ void k_loop(float (&acc)[2][4], const uint8_t* codes0
     }
 }
 
-// ------------------------------------------------------------------ router
-// logits[t, e] = x[t] . Wg[e] (e < E); gate_logit[t] = x[t] . gs (row E). CTA =
-// 8 rows (a warp each) x 16 tokens; a lane holds its 16-byte chunks of the row as
-// fp32 and reads the tokens' chunks from shared memory (consecutive lanes,
-// consecutive 16 bytes: conflict-free).
+// ------------------------------------------------------------------ router + route
+// logits[t, e] = x[t] . Wg[e] (e < E); gate_logit[t] = x[t] . gs (row E). CTA
+// (bx, by) = 8 rows (a warp each) x the 16 tokens of block by; a lane holds its
+// 16-byte chunks of the row as fp32 and reads the tokens' chunks from shared
+// memory (consecutive lanes, consecutive 16 bytes: conflict-free). Then a ticket
+// per token block: the CTA that finishes last takes the top-k of those tokens, and
+// the token block that finishes last builds the lists. Nothing waits: a CTA that
+// is not last simply exits, and the last one resets its counter for the next call.
 __global__ void __launch_bounds__(kThreads)
-router_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restrict__ gs,
-                 const uint16_t* __restrict__ x, int T, int E, int H, float* __restrict__ logits,
-                 float* __restrict__ gate_logit) {
+router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restrict__ gs,
+                       const uint16_t* __restrict__ x, int T, int E, int H, int k, float* logits,
+                       float* gate_logit, int32_t* ids, float* w, int32_t* ids_out, float* w_out,
+                       int32_t* offsets, int32_t* token_list, int32_t* active, int32_t* pass_map,
+                       WsHeader* hdr) {
     extern __shared__ uint4 xs4[];
+    __shared__ ListsSmem S;
+    __shared__ int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = H >> 3;
     const int rows = E + (gs ? 1 : 0);
@@ -154,56 +181,79 @@ router_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restrict__ g
     for (int i = threadIdx.x; i < tc * nch; i += kThreads)
         xs4[i] = *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + 8 * (size_t)i);
     __syncthreads();
-    if (r >= rows) return;
-    const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
-    float acc[kRouterTok];
+    if (r < rows) {
+        const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
+        float acc[kRouterTok];
 #pragma unroll
-    for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
-    for (int g0 = 0; g0 < nch; g0 += 256) {          // 8 chunks per lane per group
-        float wf[8][8];
+        for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
+        for (int g0 = 0; g0 < nch; g0 += 256) {          // 8 chunks per lane per group
+            float wf[8][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = g0 + lane + 32 * i;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (c < nch) v = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
-            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < 8; ++i) {
+                const int c = g0 + lane + 32 * i;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (c < nch) v = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
+                const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                wf[i][2 * p] = bf16lo(ww[p]);
-                wf[i][2 * p + 1] = bf16hi(ww[p]);
+                for (int p = 0; p < 4; ++p) {
+                    wf[i][2 * p] = bf16lo(ww[p]);
+                    wf[i][2 * p + 1] = bf16hi(ww[p]);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kRouterTok; ++t) {
+                if (t < tc) {
+                    float a = acc[t];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = g0 + lane + 32 * i;
+                        if (c < nch) {
+                            const uint4 xv = xs4[t * nch + c];
+                            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
+                                a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
+                            }
+                        }
+                    }
+                    acc[t] = a;
+                }
             }
         }
 #pragma unroll
         for (int t = 0; t < kRouterTok; ++t) {
             if (t < tc) {
-                float a = acc[t];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = g0 + lane + 32 * i;
-                    if (c < nch) {
-                        const uint4 xv = xs4[t * nch + c];
-                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
-                            a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
-                        }
-                    }
+                const float v = warp_sum(acc[t]);
+                if (lane == 0) {
+                    if (r < E) logits[(size_t)(t0 + t) * E + r] = v;
+                    else gate_logit[t0 + t] = v;
                 }
-                acc[t] = a;
             }
         }
     }
-#pragma unroll
-    for (int t = 0; t < kRouterTok; ++t) {
-        if (t < tc) {
-            const float v = warp_sum(acc[t]);
-            if (lane == 0) {
-                if (r < E) logits[(size_t)(t0 + t) * E + r] = v;
-                else gate_logit[t0 + t] = v;
-            }
-        }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&hdr->route_tickets[blockIdx.y], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int t = t0 + warp; t < t0 + tc; t += kWarps) {
+        const size_t o = (size_t)t * k;
+        topk_bitonic_warp(logits + (size_t)t * E, E, k, ids + o, w + o, ids_out ? ids_out + o : nullptr,
+                          w_out ? w_out + o : nullptr);
     }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicExch(&hdr->route_tickets[blockIdx.y], 0u);
+        s_last = atomicAdd(&hdr->route_tickets[4], 1u) == gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
+    if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[4], 0u);
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -431,20 +481,17 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
     uint16_t* hs = reinterpret_cast<uint16_t*>(ws.hs);
     float* P = ws.part;
     float* Ps = shared ? ws.part + (size_t)T * d.k * d.H : nullptr;
-    {   // 1. router GEMV (+ the shared gate's pre-activation)
+    {   // 1. router GEMV (+ the shared gate's pre-activation), top-k, lists, pass map
         const int rows = d.E + (shared ? 1 : 0);
         const dim3 grid((rows + kWarps - 1) / kWarps, (T + kRouterTok - 1) / kRouterTok);
         const size_t smem = (size_t)(T < kRouterTok ? T : kRouterTok) * d.H * 2;
-        err = cudaFuncSetAttribute(router_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = cudaFuncSetAttribute(router_route_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        router_mt_kernel<<<grid, kThreads, smem, s>>>(d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E,
-                                                      d.H, ws.logits, ws.gate_logit);
+        router_route_mt_kernel<<<grid, kThreads, smem, s>>>(
+            d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E, d.H, d.k, ws.logits, ws.gate_logit, ws.ids,
+            ws.w, ids_out, w_out, ws.offsets, ws.token_list, ws.active, ws.pass_map, ws.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    // 2. top-k, lists, active experts and the pass map (one block)
-    if ((err = launch_route_mt(ws.logits, T, d.E, d.k, ws.ids, ws.w, ids_out, w_out, ws.offsets,
-                               ws.token_list, ws.active, ws.pass_map, s)) != cudaSuccess)
-        return err;
     {   // 3. gate/up + SwiGLU
         const size_t smem = (size_t)kPass * d.H * 2;
         err = cudaFuncSetAttribute(gateup_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -25,10 +25,6 @@ cudaError_t launch_route_lists(const int32_t* ids, int total, int E, int32_t* of
                                int32_t* token_list, int32_t* active, cudaStream_t s);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          int32_t* offsets, int32_t* token_list, cudaStream_t s);
-// Fused top-k + lists + active list + pass map for T*k <= 512 (one block).
-cudaError_t launch_route_mt(const float* logits, int T, int E, int k, int32_t* ids, float* w,
-                            int32_t* ids_out, float* w_out, int32_t* offsets, int32_t* token_list,
-                            int32_t* active, int32_t* pass_map, cudaStream_t s);
 
 // Workspace of one layer call (device scratch carved from the caller's buffer).
 struct LayerWs {

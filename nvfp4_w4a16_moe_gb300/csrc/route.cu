@@ -128,87 +128,6 @@ route_lists_kernel(const int32_t* __restrict__ ids, int total, int E,
     }
 }
 
-// Fused route for up to 64 tokens (T*k <= 512 entries, E <= 256): top-k per
-// token, then the per-expert lists, the active-expert list and the pass map of
-// the multi-token decode kernels, in one block. Entry i = t*k + j goes to
-// offsets[e] + (number of entries i' < i of expert e), read off a per-expert bit
-// mask of entries: the same stable order as the counting sort above. Pass map:
-// pass_map[0] = number of passes P; pass_map[1 + p] = (active slot << 8) | pass,
-// a pass being up to kMtPass consecutive entries of one expert's list.
-constexpr int kMtRouteThreads = 512;
-constexpr int kMtMaxEntries = 512;
-constexpr int kMtPass = 16;
-
-__global__ void __launch_bounds__(kMtRouteThreads)
-route_mt_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
-                float* __restrict__ w, int32_t* __restrict__ ids_out, float* __restrict__ w_out,
-                int32_t* __restrict__ offsets, int32_t* __restrict__ token_list,
-                int32_t* __restrict__ active, int32_t* __restrict__ pass_map) {
-    __shared__ uint32_t mask[NVFP4_MAX_EXPERTS][kMtMaxEntries / 32];
-    __shared__ int s_ids[kMtMaxEntries];
-    __shared__ int s_off[NVFP4_MAX_EXPERTS];
-    __shared__ int wsum[3][NVFP4_MAX_EXPERTS / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int total = T * k;
-    const int nw = (total + 31) >> 5;
-    for (int i = tid; i < NVFP4_MAX_EXPERTS * (kMtMaxEntries / 32); i += kMtRouteThreads)
-        (&mask[0][0])[i] = 0u;
-    for (int t = warp; t < T; t += kMtRouteThreads / 32)
-        topk_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
-    __syncthreads();
-    if (tid < total) {
-        const int e = ids[tid];
-        s_ids[tid] = e;
-        atomicOr(&mask[e][tid >> 5], 1u << (tid & 31));
-        if (ids_out) ids_out[tid] = e;
-        if (w_out) w_out[tid] = w[tid];
-    }
-    __syncthreads();
-    // per-expert count c, then exclusive scans over experts (threads 0..255) of
-    // c (list offset), [c > 0] (active slot) and ceil(c / kMtPass) (first pass)
-    int c = 0;
-    if (tid < E)
-        for (int qq = 0; qq < nw; ++qq) c += __popc(mask[tid][qq]);
-    const int v0 = c, v1 = c > 0 ? 1 : 0, v2 = (c + kMtPass - 1) / kMtPass;
-    int i0 = v0, i1 = v1, i2 = v2;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n0 = __shfl_up_sync(0xffffffffu, i0, o);
-        const int n1 = __shfl_up_sync(0xffffffffu, i1, o);
-        const int n2 = __shfl_up_sync(0xffffffffu, i2, o);
-        if (lane >= o) { i0 += n0; i1 += n1; i2 += n2; }
-    }
-    if (warp < NVFP4_MAX_EXPERTS / 32 && lane == 31) {
-        wsum[0][warp] = i0;
-        wsum[1][warp] = i1;
-        wsum[2][warp] = i2;
-    }
-    __syncthreads();
-    if (tid < E) {
-        int b0 = 0, b1 = 0, b2 = 0;
-        for (int ww = 0; ww < warp; ++ww) { b0 += wsum[0][ww]; b1 += wsum[1][ww]; b2 += wsum[2][ww]; }
-        const int off = b0 + i0 - v0, slot = b1 + i1 - v1, pass0 = b2 + i2 - v2;
-        s_off[tid] = off;
-        offsets[tid] = off;
-        if (c > 0) {
-            active[1 + slot] = tid;
-            for (int pi = 0; pi < v2; ++pi) pass_map[1 + pass0 + pi] = (slot << 8) | pi;
-        }
-        if (tid == E - 1) {
-            offsets[E] = off + c;
-            active[0] = slot + v1;
-            pass_map[0] = pass0 + v2;
-        }
-    }
-    __syncthreads();
-    if (tid < total) {
-        const int e = s_ids[tid], qw = tid >> 5;
-        int r = __popc(mask[e][qw] & ((1u << (tid & 31)) - 1u));
-        for (int qq = 0; qq < qw; ++qq) r += __popc(mask[e][qq]);
-        token_list[s_off[e] + r] = tid;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_route_lists(const int32_t* ids, int total, int E, int32_t* offsets,
@@ -233,15 +152,6 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
     cudaError_t err = launch_route_topk(logits, T, E, k, ids, w, s);
     if (err != cudaSuccess) return err;
     return launch_route_lists(ids, T * k, E, offsets, token_list, nullptr, s);
-}
-
-cudaError_t launch_route_mt(const float* logits, int T, int E, int k, int32_t* ids, float* w,
-                            int32_t* ids_out, float* w_out, int32_t* offsets, int32_t* token_list,
-                            int32_t* active, int32_t* pass_map, cudaStream_t s) {
-    if (T < 1 || T * k > kMtMaxEntries || E > NVFP4_MAX_EXPERTS) return cudaErrorInvalidValue;
-    route_mt_kernel<<<1, kMtRouteThreads, 0, s>>>(logits, T, E, k, ids, w, ids_out, w_out, offsets,
-                                                  token_list, active, pass_map);
-    return cudaGetLastError();
 }
 
 }  // namespace nvfp4
