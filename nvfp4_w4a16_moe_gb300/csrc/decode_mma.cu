@@ -1,6 +1,6 @@
 // MoE layer, multi-token decode (1..64 tokens per call, E4M3 block scales): router
-// GEMV, fused route, grouped gate/up + SwiGLU and grouped down on the warp-level
-// tensor cores, then the routing-weighted combine.
+// GEMV with the fused route, grouped gate/up + SwiGLU and grouped down on the
+// warp-level tensor cores, then the routing-weighted combine.
 //
 // Sources (page title, section):
 //  - lynn-engine tutorials index, row 06 "MoE router" (softmax over all experts ->
@@ -12,11 +12,22 @@
 //
 // Each routed expert with n entries, and the shared expert (whose entries are the T
 // tokens), is a small GEMM: weight rows times up to 16 entries per pass. The weight
-// rows sit on the M side of mma.sync m16n8k16 (bf16 in, fp32 accumulate), the
+// rows sit on the M side of mma.sync m16n8k16 (f16 in, fp32 accumulate), the
 // entries on its N side (one or two n8 blocks). The NVFP4 codes go from HBM into
-// registers and are expanded there, exactly, into the A fragments: no shared-memory
-// round trip and no bf16 copy of a weight. The entries' bf16 rows (x for gate/up,
-// h for down) are staged once per CTA in shared memory and read as B fragments.
+// registers and are expanded there into the A fragments: cvt gives the E2M1 codes
+// as f16 and one f16x2 multiply applies the E4M3 block scale; the product has at
+// most 6 significant bits and lies in [2^-10, 2688], so it is exact. No shared-memory
+// round trip, no copy of a weight.
+//
+// Operand B is the entries' activation rows (x for gate/up, h for down), staged
+// once per CTA in shared memory as f16. Each row is first multiplied by 2^k_r, the
+// power of two that puts its largest magnitude in [2^14, 2^15): no f16 overflow
+// for any bf16 or fp32 input, and every element within 2^-28 of the row's largest
+// converts exactly (a bf16 has 8 significant bits, f16 11); smaller elements carry
+// an absolute error below 2^-39 of the row's largest. The epilogue multiplies the
+// fp32 accumulator by 2^-k_r (exact). Row maxima come from the router kernel (x)
+// and from the gate/up epilogue (h, an atomicMax over bit patterns of non-negative
+// floats: order-independent, so deterministic).
 //
 // K order. A contraction may visit K in any order as long as both operands use the
 // same one. In 256-element chunk j, the lanes of quad position q (lane % 4) own the
@@ -43,29 +54,32 @@ constexpr int kMaxDim = 4096;      // H, I, Is bound of this path (shared-memory
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
                  "{%8,%9}, {%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Staged row r, 8-byte unit u (four bf16) lives at unit u ^ (((u >> 2) & 12) | (r & 3)).
+// Row scaling: k with max|row| * 2^k in [2^14, 2^15), from the fp32 bits of max|row|
+// (0 for an all-zero row; clamped to [-110, 110] so that 2^k and 2^-k are normal).
+__device__ __forceinline__ int row_shift(uint32_t amax_bits) {
+    if (amax_bits == 0u) return 0;
+    const int e = (int)(amax_bits >> 23) - 127;
+    return min(110, max(-110, 14 - e));
+}
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((k + 127) << 23); }
+
+// Two fp32 -> f16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Staged row r, 8-byte unit u (four f16) lives at unit u ^ (((u >> 2) & 12) | (r & 3)).
 // In one MMA step the 16 lanes of a half-warp (rows r & 3 = g & 3, quads q) read
 // units whose low four bits are s ^ (4q | (g & 3)): 16 distinct bank pairs.
 __device__ __forceinline__ uint32_t swz(uint32_t u, uint32_t r) { return u ^ (((u >> 2) & 12u) | (r & 3u)); }
-
-// Copy n bf16 rows of K elements (row r from row_ptr(r)) into the swizzled layout.
-template <class RowPtr>
-__device__ __forceinline__ void stage_rows(uint8_t* sm, int n, int K, RowPtr row_ptr) {
-    const int per_row = K >> 3;   // 16-byte granules = two units
-    for (int i = threadIdx.x; i < n * per_row; i += kThreads) {
-        const int r = i / per_row, v = i - r * per_row;
-        const uint4 val = *reinterpret_cast<const uint4*>(row_ptr(r) + 8 * (size_t)v);
-        uint2* dst = reinterpret_cast<uint2*>(sm + (size_t)r * K * 2);
-        dst[swz(2 * v, r)] = make_uint2(val.x, val.y);
-        dst[swz(2 * v + 1, r)] = make_uint2(val.z, val.w);
-    }
-}
 
 // One weight row's share of a chunk for one lane: 32 code bytes and 4 E4M3 scales.
 struct WChunk {
@@ -81,11 +95,15 @@ __device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t
     return c;
 }
 
-// Four E2M1 code bytes (one 32-bit word, two MMA steps of one weight row) ->
-// four bf16x2 of code * scale. The word is unpacked into byte registers for cvt
-// (no shifts); the f16 -> bf16 re-reading (magnitude >> 3, sign kept, see
-// e2m1x2_to_bf16x2_scaled) takes its shift as a 32x32 -> high-32 multiply by
-// 2^29, which runs on the FMA pipe instead of the integer ALU.
+// E4M3 block scale -> f16x2 {scale, scale} (exact).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t byte) {
+    uint32_t r;
+    asm("{\n .reg .b16 b;\n cvt.u16.u32 b, %1;\n cvt.rn.f16x2.e4m3x2 %0, b;\n}" : "=r"(r) : "r"(byte * 0x101u));
+    return r;
+}
+
+// Four E2M1 code bytes (one 32-bit word: two MMA steps of one weight row) -> four
+// f16x2 of code * scale. The word is unpacked into byte registers for cvt.
 __device__ __forceinline__ void expand_word(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
     uint32_t h[4];
     asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
@@ -93,10 +111,7 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t s2, uint32_t (&
         " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
         : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t m = __umulhi(h[b] & 0x7FFF7FFFu, 1u << 29) | (h[b] & 0x80008000u);
-        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(m), "r"(s2));
-    }
+    for (int b = 0; b < 4; ++b) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(h[b]), "r"(s2));
 }
 
 __device__ __forceinline__ uint32_t word_of(const WChunk& c, int wi) {
@@ -115,8 +130,8 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[2][4], const WChunk& c0, 
     uint32_t s0[4], s1[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        s0[b] = e4m3_to_bf16x2_x2p112((c0.sc >> (8 * b)) & 0xFFu);
-        s1[b] = e4m3_to_bf16x2_x2p112((c1.sc >> (8 * b)) & 0xFFu);
+        s0[b] = e4m3_to_f16x2_dup((c0.sc >> (8 * b)) & 0xFFu);
+        s1[b] = e4m3_to_f16x2_dup((c1.sc >> (8 * b)) & 0xFFu);
     }
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
@@ -168,7 +183,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
                        const uint16_t* __restrict__ x, int T, int E, int H, int k, float* logits,
                        float* gate_logit, int32_t* ids, float* w, int32_t* ids_out, float* w_out,
                        int32_t* offsets, int32_t* token_list, int32_t* active, int32_t* pass_map,
-                       WsHeader* hdr) {
+                       uint32_t* amax, WsHeader* hdr) {
     extern __shared__ uint4 xs4[];
     __shared__ ListsSmem S;
     __shared__ int s_last;
@@ -181,16 +196,34 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     for (int i = threadIdx.x; i < tc * nch; i += kThreads)
         xs4[i] = *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + 8 * (size_t)i);
     __syncthreads();
-    if (r < rows) {
-        const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
-        float acc[kRouterTok];
+    if (blockIdx.x == 0) {
+        // max |x| of each token of the block (bf16 magnitudes order as integers),
+        // stored as fp32 bits; block (0, 0) also clears the h row maxima that the
+        // gate/up kernel accumulates
+        for (int t = warp; t < tc; t += kWarps) {
+            uint32_t m = 0u;
+            for (int c = lane; c < nch; c += 32) {
+                const uint4 v = xs4[t * nch + c];
+                const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
-        for (int g0 = 0; g0 < nch; g0 += 256) {          // 8 chunks per lane per group
+                for (int p = 0; p < 4; ++p) m = max(m, max(ww[p] & 0x7FFFu, (ww[p] >> 16) & 0x7FFFu));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) amax[t0 + t] = m << 16;
+        }
+        if (blockIdx.y == 0)
+            for (int i = threadIdx.x; i < T * k + T; i += kThreads) amax[T + i] = 0u;
+    }
+    if (r < rows) {
+        // one token at a time (a rolled loop keeps the code small: this kernel runs
+        // once per SM, so its instructions are fetched cold)
+        const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
+        if (nch <= 256) {
             float wf[8][8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int c = g0 + lane + 32 * i;
+                const int c = lane + 32 * i;
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (c < nch) v = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
                 const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
@@ -200,34 +233,48 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
                     wf[i][2 * p + 1] = bf16hi(ww[p]);
                 }
             }
+#pragma unroll 1
+            for (int t = 0; t < tc; ++t) {
+                float a = 0.f;
 #pragma unroll
-            for (int t = 0; t < kRouterTok; ++t) {
-                if (t < tc) {
-                    float a = acc[t];
+                for (int i = 0; i < 8; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < nch) {
+                        const uint4 xv = xs4[t * nch + c];
+                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = g0 + lane + 32 * i;
-                        if (c < nch) {
-                            const uint4 xv = xs4[t * nch + c];
-                            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                            for (int p = 0; p < 4; ++p) {
-                                a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
-                                a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
-                            }
+                        for (int p = 0; p < 4; ++p) {
+                            a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
+                            a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
                         }
                     }
-                    acc[t] = a;
+                }
+                a = warp_sum(a);
+                if (lane == 0) {
+                    if (r < E) logits[(size_t)(t0 + t) * E + r] = a;
+                    else gate_logit[t0 + t] = a;
                 }
             }
-        }
+        } else {
+#pragma unroll 1
+            for (int t = 0; t < tc; ++t) {
+                float a = 0.f;
+#pragma unroll 1
+                for (int c = lane; c < nch; c += 32) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + 8 * (size_t)c));
+                    const uint4 xv = xs4[t * nch + c];
+                    const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-        for (int t = 0; t < kRouterTok; ++t) {
-            if (t < tc) {
-                const float v = warp_sum(acc[t]);
+                    for (int p = 0; p < 4; ++p) {
+                        a = fmaf(bf16lo(ww[p]), bf16lo(xx[p]), a);
+                        a = fmaf(bf16hi(ww[p]), bf16hi(xx[p]), a);
+                    }
+                }
+                a = warp_sum(a);
                 if (lane == 0) {
-                    if (r < E) logits[(size_t)(t0 + t) * E + r] = v;
-                    else gate_logit[t0 + t] = v;
+                    if (r < E) logits[(size_t)(t0 + t) * E + r] = a;
+                    else gate_logit[t0 + t] = a;
                 }
             }
         }
@@ -262,13 +309,17 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
 // expert's pass pi is tokens [16 pi, 16 pi + 16). Warp w takes gate rows
 // i0 + 8w + g as fragment rows 0-7 and the matching up rows as rows 8-15, so lane
 // (g, q) ends with gate and up of row i0 + 8w + g for entries 2q, 2q+1 of each n8
-// block: h = silu(ts_g * gate) * (ts_u * up), written as bf16.
+// block: h = silu(ts_g * gate) * (ts_u * up), written in fp32 (entry-major [T*k, I]
+// for the routed experts, [T, Is] for the shared one). hmax keeps each h row's
+// largest magnitude (routed entry e at e, shared token t at T*k + t).
 __global__ void __launch_bounds__(kThreads, 3)
 gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ token_list,
                  const int32_t* __restrict__ active, const int32_t* __restrict__ pass_map,
-                 uint16_t* __restrict__ h, uint16_t* __restrict__ hs) {
+                 const uint32_t* __restrict__ xmax, uint32_t* __restrict__ hmax, float* __restrict__ h,
+                 float* __restrict__ hs) {
     extern __shared__ __align__(16) uint8_t stage[];
+    __shared__ uint32_t s_hmax[kPass];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
     const int H = d.H, k = d.k;
@@ -283,7 +334,7 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         const int32_t* list;   // routed: the pass's entries; shared: none (tokens first + r)
         float tsg, tsu;
         int Irows, i0, n, first;
-        uint16_t* out;
+        float* out;
         if (item < items_r) {
             const int p = item / rb_r;
             const int pm = pass_map[1 + p];
@@ -313,14 +364,32 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
             tsu = __ldg(d.sh_gu_tscale + 1);
             out = hs;
         }
+        // entry r of the pass: its token, its h row, its slot in hmax
+        auto tok = [&](int r) { return list ? list[r] / k : first + r; };
+        auto hrow = [&](int r) { return list ? list[r] : first + r; };
+        auto hidx = [&](int r) { return list ? list[r] : T * k + first + r; };
         const int i = i0 + 8 * warp + (int)g;
         const uint8_t* cg = codes + (size_t)i * (H / 2) + 32 * q;
         const uint8_t* cu = codes + (size_t)(Irows + i) * (H / 2) + 32 * q;
         const uint8_t* sg = scl + (size_t)i * (H / 16) + 4 * q;
         const uint8_t* su = scl + (size_t)(Irows + i) * (H / 16) + 4 * q;
         const WChunk c0 = load_chunk(cg, sg, 0), c1 = load_chunk(cu, su, 0);
-        __syncthreads();   // the previous item's MMAs are done with the stage
-        stage_rows(stage, n, H, [&](int r) { return x + (size_t)(list ? list[r] / k : first + r) * H; });
+        __syncthreads();   // the previous item is done with the stage and s_hmax
+        if (threadIdx.x < kPass) s_hmax[threadIdx.x] = 0u;
+        {   // x rows of the entries, times 2^k_t, as f16
+            const int per_row = H >> 3;
+            for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
+                const int r = idx / per_row, v = idx - r * per_row;
+                const int t = tok(r);
+                const float sc = exp2i(row_shift(__ldg(xmax + t)));
+                const uint4 val = *reinterpret_cast<const uint4*>(x + (size_t)t * H + 8 * (size_t)v);
+                uint2* dst = reinterpret_cast<uint2*>(stage + (size_t)r * H * 2);
+                dst[swz(2 * v, r)] = make_uint2(f16x2_of(bf16lo(val.x) * sc, bf16hi(val.x) * sc),
+                                                f16x2_of(bf16lo(val.y) * sc, bf16hi(val.y) * sc));
+                dst[swz(2 * v + 1, r)] = make_uint2(f16x2_of(bf16lo(val.z) * sc, bf16hi(val.z) * sc),
+                                                    f16x2_of(bf16lo(val.w) * sc, bf16hi(val.w) * sc));
+            }
+        }
         __syncthreads();
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * H * 2;
@@ -332,32 +401,44 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int r = 8 * nb + 2 * (int)q + c;
+                uint32_t m = 0u;
                 if (r < n) {
-                    const float gv = acc[nb][c] * tsg, uv = acc[nb][2 + c] * tsu;
-                    const size_t row = list ? (size_t)list[r] : (size_t)(first + r);
-                    out[row * Irows + i] = f32_to_bf16(silu_f32(gv) * uv);
+                    const float inv = exp2i(-row_shift(__ldg(xmax + tok(r))));
+                    const float gv = acc[nb][c] * inv * tsg, uv = acc[nb][2 + c] * inv * tsu;
+                    const float hv = silu_f32(gv) * uv;
+                    out[(size_t)hrow(r) * Irows + i] = hv;
+                    m = __float_as_uint(fabsf(hv));
                 }
+                // largest |h| of entry r over the warp's eight rows (lanes sharing q)
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                if (g == 0 && r < n) atomicMax(&s_hmax[r], m);
             }
         }
+        __syncthreads();
+        if (threadIdx.x < n) atomicMax(&hmax[hidx(threadIdx.x)], s_hmax[threadIdx.x]);
     }
 }
 
 // ------------------------------------------------------------------ down
 // Item = (slot pass, block of 128 output rows). Warp w takes rows
 // nr = 128 rb + 16w + g (fragment rows 0-7) and nr + 8 (rows 8-15) over K = I
-// (Is for the shared expert). Output rows, fp32, one writer each:
+// (Is for the shared expert); the entries' h rows are staged as f16 times 2^k_h.
+// Output rows, fp32, one writer each:
 //   P[entry, n] = w_entry * ts_e * (D_e[n] . h_entry)          (routed)
 //   Ps[t, n]    = sigmoid(gate_t) * ts_s * (Ds[n] . hs_t)       (shared)
 __global__ void __launch_bounds__(kThreads, 3)
 down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
                const int32_t* __restrict__ token_list, const int32_t* __restrict__ active,
                const int32_t* __restrict__ pass_map, const float* __restrict__ wts,
-               const float* __restrict__ gate_logit, const uint16_t* __restrict__ h,
-               const uint16_t* __restrict__ hs, float* __restrict__ P, float* __restrict__ Ps) {
+               const float* __restrict__ gate_logit, const float* __restrict__ h,
+               const float* __restrict__ hs, const uint32_t* __restrict__ hmax, float* __restrict__ P,
+               float* __restrict__ Ps) {
     extern __shared__ __align__(16) uint8_t stage[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
-    const int H = d.H;
+    const int H = d.H, k = d.k;
     const int rb_n = H / kDnRows;
     const int items_r = pass_map[0] * rb_n;
     const int items = items_r + (d.Is > 0 ? (T + kPass - 1) / kPass * rb_n : 0);
@@ -366,7 +447,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         const uint8_t* codes;
         const uint8_t* scl;
         const int32_t* list;
-        const uint16_t* src;
+        const float* src;
         float ts;
         int K, n, first, rb;
         if (item < items_r) {
@@ -396,6 +477,8 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
             ts = __ldg(d.sh_dn_tscale);
             src = hs;
         }
+        auto hrow = [&](int r) { return list ? list[r] : first + r; };
+        auto hidx = [&](int r) { return list ? list[r] : T * k + first + r; };
         const int nr = rb * kDnRows + 16 * warp + (int)g;
         const uint8_t* c0p = codes + (size_t)nr * (K / 2) + 32 * q;
         const uint8_t* c1p = codes + (size_t)(nr + 8) * (K / 2) + 32 * q;
@@ -403,7 +486,16 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         const uint8_t* s1p = scl + (size_t)(nr + 8) * (K / 16) + 4 * q;
         const WChunk c0 = load_chunk(c0p, s0p, 0), c1 = load_chunk(c1p, s1p, 0);
         __syncthreads();
-        stage_rows(stage, n, K, [&](int r) { return src + (size_t)(list ? list[r] : first + r) * K; });
+        {   // h rows of the entries, times 2^k_h, as f16
+            const int per_row = K >> 2;
+            for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
+                const int r = idx / per_row, v = idx - r * per_row;
+                const float sc = exp2i(row_shift(__ldg(hmax + hidx(r))));
+                const float4 f = *reinterpret_cast<const float4*>(src + (size_t)hrow(r) * K + 4 * (size_t)v);
+                reinterpret_cast<uint2*>(stage + (size_t)r * K * 2)[swz(v, r)] =
+                    make_uint2(f16x2_of(f.x * sc, f.y * sc), f16x2_of(f.z * sc, f.w * sc));
+            }
+        }
         __syncthreads();
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * K * 2;
@@ -416,14 +508,15 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
             for (int c = 0; c < 2; ++c) {
                 const int r = 8 * nb + 2 * (int)q + c;
                 if (r < n) {
+                    const float inv = exp2i(-row_shift(__ldg(hmax + hidx(r))));
                     if (list) {
                         const int en = list[r];
-                        const float f = wts[en] * ts;
+                        const float f = inv * wts[en] * ts;
                         P[(size_t)en * H + nr] = acc[nb][c] * f;
                         P[(size_t)en * H + nr + 8] = acc[nb][2 + c] * f;
                     } else {
                         const int t = first + r;
-                        const float f = sigmoid_f32(gate_logit[t]) * ts;
+                        const float f = inv * sigmoid_f32(gate_logit[t]) * ts;
                         Ps[(size_t)t * H + nr] = acc[nb][c] * f;
                         Ps[(size_t)t * H + nr + 8] = acc[nb][2 + c] * f;
                     }
@@ -477,8 +570,10 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
     const bool shared = d.Is > 0;
     const int passes_shared = (T + kPass - 1) / kPass;
     const int passes_routed_ub = (d.E < T * d.k ? d.E : T * d.k) + T * d.k / kPass;
-    uint16_t* h = reinterpret_cast<uint16_t*>(ws.h);
-    uint16_t* hs = reinterpret_cast<uint16_t*>(ws.hs);
+    float* h = ws.h;
+    float* hs = ws.hs;
+    uint32_t* xmax = ws.amax;
+    uint32_t* hmax = ws.amax + T;
     float* P = ws.part;
     float* Ps = shared ? ws.part + (size_t)T * d.k * d.H : nullptr;
     {   // 1. router GEMV (+ the shared gate's pre-activation), top-k, lists, pass map
@@ -489,7 +584,7 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
         if (err != cudaSuccess) return err;
         router_route_mt_kernel<<<grid, kThreads, smem, s>>>(
             d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E, d.H, d.k, ws.logits, ws.gate_logit, ws.ids,
-            ws.w, ids_out, w_out, ws.offsets, ws.token_list, ws.active, ws.pass_map, ws.hdr);
+            ws.w, ids_out, w_out, ws.offsets, ws.token_list, ws.active, ws.pass_map, ws.amax, ws.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 3. gate/up + SwiGLU
@@ -501,7 +596,7 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
         const long cap = (long)dev.num_sms * resident_ctas((const void*)gateup_mt_kernel, smem);
         const int grid = (int)(items_ub < cap ? items_ub : cap);
         gateup_mt_kernel<<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
-                                                      ws.pass_map, h, hs);
+                                                      ws.pass_map, xmax, hmax, h, hs);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 4. down, weighted rows
@@ -513,7 +608,7 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
         const long cap = (long)dev.num_sms * resident_ctas((const void*)down_mt_kernel, smem);
         const int grid = (int)(items_ub < cap ? items_ub : cap);
         down_mt_kernel<<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active, ws.pass_map,
-                                                    ws.w, ws.gate_logit, h, hs, P, Ps);
+                                                    ws.w, ws.gate_logit, h, hs, hmax, P, Ps);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 5. combine

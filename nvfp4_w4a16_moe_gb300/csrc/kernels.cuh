@@ -41,6 +41,7 @@ struct LayerWs {
     unsigned long long* words;  // [E + 2 + k*I + Is] (launch tag, value) words of the one-launch kernel
     int32_t* pass_map;    // [E + T*k + 2]  pass_map[0] = P, then (active slot << 8) | pass
     float* part;          // [T*k + T, H]  weighted routed rows, then the shared rows
+    uint32_t* amax;       // [T + T*k + T] max |x| of each token, then max |h| of each h row (fp32 bits)
     size_t bytes;
 };
 

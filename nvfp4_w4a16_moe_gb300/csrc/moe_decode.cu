@@ -357,6 +357,7 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T) {
     b += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
     b += align256(sizeof(int32_t) * (Tk + d.E + 2));
     b += align256(sizeof(float) * (Tk + T) * d.H);
+    b += align256(sizeof(uint32_t) * (Tk + 2 * (size_t)T));
     return b;
 }
 
@@ -378,6 +379,7 @@ LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T) {
     p += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
     w.pass_map = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * (Tk + d.E + 2));
     w.part = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (Tk + T) * d.H);
+    w.amax = reinterpret_cast<uint32_t*>(p); p += align256(sizeof(uint32_t) * (Tk + 2 * (size_t)T));
     w.bytes = (size_t)(p - static_cast<char*>(base));
     return w;
 }

@@ -62,7 +62,7 @@ __device__ __forceinline__ void topk_bitonic_warp(const float* lg, int E, int k,
             }
         }
     }
-#pragma unroll
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
         float pv[8];
         int pe[8];
