@@ -15,15 +15,17 @@ namespace nvfp4 {
 // Every workspace starts with this header. `status` holds an nvfp4_status the
 // device recorded; `barrier` counts grid-barrier arrivals monotonically across
 // launches (one 64-bit counter never wraps in practice); `route_tickets` count
-// the router blocks of one multi-token call that are done (per 16-token block,
-// then over token blocks) and are reset to 0 by the block that finishes last.
+// the router blocks of one multi-token call that are done (one counter per token
+// block, then one over token blocks) and are reset to 0 by the block that
+// finishes last.
+constexpr int kRouteTicketBlocks = 8;
 struct alignas(256) WsHeader {
     uint32_t status;
     uint32_t pad0;
     unsigned long long barrier;
     unsigned int amax_bits;      // nvfp4_pack: max |w| as fp32 bits
-    unsigned int route_tickets[5];
-    unsigned int pad1[54];
+    unsigned int route_tickets[kRouteTicketBlocks + 1];
+    unsigned int pad1[50];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -129,6 +131,26 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
     uint2 v;
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
                  : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// Streamed weights with an L2 evict-first policy: they are read once per call,
+// so they should not push the code, the routing arrays and the activations out
+// of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_stream_v4_ef(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32_ef(const void* p, uint64_t pol) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
     return v;
 }
 

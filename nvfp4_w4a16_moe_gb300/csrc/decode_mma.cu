@@ -49,8 +49,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPass = 16;          // entries per pass: two n8 MMA blocks
 constexpr int kGuPairs = 64;       // gate/up row pairs per CTA item (8 per warp)
 constexpr int kDnRows = 128;       // down output rows per CTA item (16 per warp)
-constexpr int kRouterTok = 16;     // tokens per router CTA
+constexpr int kRouterTok = 8;      // tokens per router CTA (the last CTA of a block: one warp per token)
 constexpr int kMaxDim = 4096;      // H, I, Is bound of this path (shared-memory staging)
+static_assert(NVFP4_DECODE_MAX_TOKENS / kRouterTok <= kRouteTicketBlocks, "one ticket counter per token block");
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -87,11 +88,11 @@ struct WChunk {
     uint32_t sc;
 };
 
-__device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t* scl, int j) {
+__device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t* scl, int j, uint64_t pol) {
     WChunk c;
-    c.lo = ld_stream_v4(codes + 128 * j);
-    c.hi = ld_stream_v4(codes + 128 * j + 16);
-    c.sc = ld_stream_u32(scl + 16 * j);
+    c.lo = ld_stream_v4_ef(codes + 128 * j, pol);
+    c.hi = ld_stream_v4_ef(codes + 128 * j + 16, pol);
+    c.sc = ld_stream_u32_ef(scl + 16 * j, pol);
     return c;
 }
 
@@ -157,12 +158,12 @@ template <int NB>
 __device__ __forceinline__ void k_loop(float (&acc)[2][4], const uint8_t* codes0, const uint8_t* scl0,
                                        const uint8_t* codes1, const uint8_t* scl1, int nchunk,
                                        const uint8_t* brow0, const uint8_t* brow1, uint32_t q,
-                                       uint32_t xmask, WChunk c0, WChunk c1) {
+                                       uint32_t xmask, WChunk c0, WChunk c1, uint64_t pol) {
     for (int j = 0; j < nchunk; ++j) {
         WChunk n0 = c0, n1 = c1;
         if (j + 1 < nchunk) {
-            n0 = load_chunk(codes0, scl0, j + 1);
-            n1 = load_chunk(codes1, scl1, j + 1);
+            n0 = load_chunk(codes0, scl0, j + 1, pol);
+            n1 = load_chunk(codes1, scl1, j + 1, pol);
         }
         chunk_mma<NB>(acc, c0, c1, brow0, brow1, 64u * j + 16u * q, xmask);
         c0 = n0;
@@ -234,25 +235,39 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
                 }
             }
 #pragma unroll 1
-            for (int t = 0; t < tc; ++t) {
-                float a = 0.f;
+            for (int t = 0; t < tc; t += 2) {   // two tokens per pass: two independent chains
+                const bool two = t + 1 < tc;
+                float a = 0.f, b = 0.f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int c = lane + 32 * i;
                     if (c < nch) {
                         const uint4 xv = xs4[t * nch + c];
+                        const uint4 yv = two ? xs4[(t + 1) * nch + c] : make_uint4(0, 0, 0, 0);
                         const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+                        const uint32_t yy[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
                         for (int p = 0; p < 4; ++p) {
                             a = fmaf(wf[i][2 * p], bf16lo(xx[p]), a);
                             a = fmaf(wf[i][2 * p + 1], bf16hi(xx[p]), a);
+                            b = fmaf(wf[i][2 * p], bf16lo(yy[p]), b);
+                            b = fmaf(wf[i][2 * p + 1], bf16hi(yy[p]), b);
                         }
                     }
                 }
-                a = warp_sum(a);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    a += __shfl_xor_sync(0xffffffffu, a, o);
+                    b += __shfl_xor_sync(0xffffffffu, b, o);
+                }
                 if (lane == 0) {
-                    if (r < E) logits[(size_t)(t0 + t) * E + r] = a;
-                    else gate_logit[t0 + t] = a;
+                    if (r < E) {
+                        logits[(size_t)(t0 + t) * E + r] = a;
+                        if (two) logits[(size_t)(t0 + t + 1) * E + r] = b;
+                    } else {
+                        gate_logit[t0 + t] = a;
+                        if (two) gate_logit[t0 + t + 1] = b;
+                    }
                 }
             }
         } else {
@@ -287,20 +302,20 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     __threadfence();
     for (int t = t0 + warp; t < t0 + tc; t += kWarps) {
         const size_t o = (size_t)t * k;
-        topk_bitonic_warp(logits + (size_t)t * E, E, k, ids + o, w + o, ids_out ? ids_out + o : nullptr,
+        topk_warp_mt(logits + (size_t)t * E, E, k, ids + o, w + o, ids_out ? ids_out + o : nullptr,
                           w_out ? w_out + o : nullptr);
     }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         atomicExch(&hdr->route_tickets[blockIdx.y], 0u);
-        s_last = atomicAdd(&hdr->route_tickets[4], 1u) == gridDim.y - 1;
+        s_last = atomicAdd(&hdr->route_tickets[kRouteTicketBlocks], 1u) == gridDim.y - 1;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
-    if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[4], 0u);
+    if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -328,6 +343,7 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
     const int items = items_r + (T + kPass - 1) / kPass * rb_s;
     const int nchunk = H >> 8;
     const uint32_t xmask = 4u * q | (g & 3u);
+    const uint64_t pol = l2_evict_first_policy();
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const uint8_t* codes;
         const uint8_t* scl;
@@ -373,7 +389,7 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         const uint8_t* cu = codes + (size_t)(Irows + i) * (H / 2) + 32 * q;
         const uint8_t* sg = scl + (size_t)i * (H / 16) + 4 * q;
         const uint8_t* su = scl + (size_t)(Irows + i) * (H / 16) + 4 * q;
-        const WChunk c0 = load_chunk(cg, sg, 0), c1 = load_chunk(cu, su, 0);
+        const WChunk c0 = load_chunk(cg, sg, 0, pol), c1 = load_chunk(cu, su, 0, pol);
         __syncthreads();   // the previous item is done with the stage and s_hmax
         if (threadIdx.x < kPass) s_hmax[threadIdx.x] = 0u;
         {   // x rows of the entries, times 2^k_t, as f16
@@ -394,8 +410,8 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * H * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * H * 2;
-        if (n > 8) k_loop<2>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1);
-        else k_loop<1>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1);
+        if (n > 8) k_loop<2>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1, pol);
+        else k_loop<1>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1, pol);
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
@@ -443,6 +459,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
     const int items_r = pass_map[0] * rb_n;
     const int items = items_r + (d.Is > 0 ? (T + kPass - 1) / kPass * rb_n : 0);
     const uint32_t xmask = 4u * q | (g & 3u);
+    const uint64_t pol = l2_evict_first_policy();
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const uint8_t* codes;
         const uint8_t* scl;
@@ -484,7 +501,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         const uint8_t* c1p = codes + (size_t)(nr + 8) * (K / 2) + 32 * q;
         const uint8_t* s0p = scl + (size_t)nr * (K / 16) + 4 * q;
         const uint8_t* s1p = scl + (size_t)(nr + 8) * (K / 16) + 4 * q;
-        const WChunk c0 = load_chunk(c0p, s0p, 0), c1 = load_chunk(c1p, s1p, 0);
+        const WChunk c0 = load_chunk(c0p, s0p, 0, pol), c1 = load_chunk(c1p, s1p, 0, pol);
         __syncthreads();
         {   // h rows of the entries, times 2^k_h, as f16
             const int per_row = K >> 2;
@@ -500,8 +517,8 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * K * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * K * 2;
-        if (n > 8) k_loop<2>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1);
-        else k_loop<1>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1);
+        if (n > 8) k_loop<2>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
+        else k_loop<1>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll

@@ -1,6 +1,6 @@
 // Routing helpers of the multi-token decode path (T <= 64 tokens, E <= 256,
-// k <= 8): a warp top-k by bitonic merging and the block-level construction of
-// the per-expert lists, the active-expert list and the pass map.
+// k <= 8): a warp top-k and the block-level construction of the per-expert lists,
+// the active-expert list and the pass map.
 //
 // lynn-engine tutorials index, row 06 (MoE router): softmax over all experts,
 // top-k, renormalise, which equals a softmax over the k selected logits. The k
@@ -23,22 +23,25 @@ __device__ __forceinline__ bool route_before(float v, int e, float v2, int e2) {
     return v > v2 || (v == v2 && e < e2);
 }
 
+// Order (va, ea), (vb, eb) so the first comes first; selects, no branch.
 __device__ __forceinline__ void route_cas(float& va, int& ea, float& vb, int& eb) {
-    if (route_before(vb, eb, va, ea)) {
-        const float tv = va; va = vb; vb = tv;
-        const int te = ea; ea = eb; eb = te;
-    }
+    const bool sw = route_before(vb, eb, va, ea);
+    const float v0 = sw ? vb : va, v1 = sw ? va : vb;
+    const int e0 = sw ? eb : ea, e1 = sw ? ea : eb;
+    va = v0; vb = v1; ea = e0; eb = e1;
 }
 
 // Top-k of one token's E logits (lane l holds experts l, l+32, ..., l+224): each
-// lane sorts its eight, then five butterfly rounds each merge a lane's sorted
-// eight with its partner's and keep the first eight (element-wise best of one list
-// against the other reversed is a bitonic sequence holding the top eight; three
-// compare-exchange stages sort it). Every lane ends with the same sorted top
-// eight. Lane j < k writes ids[j] and w[j]. Logits are read through L2 (`ld.cg`)
-// because other blocks wrote them.
-__device__ __forceinline__ void topk_bitonic_warp(const float* lg, int E, int k, int32_t* ids,
-                                                  float* w, int32_t* ids_out, float* w_out) {
+// lane sorts its eight (bitonic network), then five butterfly rounds each merge a
+// lane's sorted eight with its partner's and keep the first eight: element-wise the
+// better of one list and the other reversed is a bitonic sequence holding the top
+// eight, and three compare-exchange stages sort it. Every lane ends with the same
+// sorted top eight. The chain of dependent steps is short (about 45 compare-
+// exchange or select levels) and branch-free; the butterfly loop stays rolled to
+// keep the code small. Lane j < k writes ids[j] and w[j]. Logits are read through
+// L2 (`ld.cg`) because other blocks wrote them.
+__device__ __forceinline__ void topk_warp_mt(const float* lg, int E, int k, int32_t* ids, float* w,
+                                             int32_t* ids_out, float* w_out) {
     const int lane = threadIdx.x & 31;
     float v[8];
     int e[8];
@@ -73,7 +76,9 @@ __device__ __forceinline__ void topk_bitonic_warp(const float* lg, int E, int k,
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            if (!route_before(v[i], e[i], pv[7 - i], pe[7 - i])) { v[i] = pv[7 - i]; e[i] = pe[7 - i]; }
+            const bool mine = route_before(v[i], e[i], pv[7 - i], pe[7 - i]);
+            v[i] = mine ? v[i] : pv[7 - i];
+            e[i] = mine ? e[i] : pe[7 - i];
         }
 #pragma unroll
         for (int stride = 4; stride > 0; stride >>= 1) {
@@ -84,21 +89,24 @@ __device__ __forceinline__ void topk_bitonic_warp(const float* lg, int E, int k,
             }
         }
     }
-    float ex[8];
-    float sum = 0.f;
+    // w_j = exp(l_j - l_max) / sum_{j' < k} exp(l_j' - l_max), summed in rank order;
+    // lane j takes element j of the (identical) lists
+    float my_v = v[0];
+    int my_e = e[0];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < k) { ex[j] = expf(v[j] - v[0]); sum += ex[j]; }
+    for (int j = 1; j < 8; ++j) {
+        if (lane == j) { my_v = v[j]; my_e = e[j]; }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < k && lane == j) {
-            const float wj = ex[j] / sum;
-            ids[j] = e[j];
-            w[j] = wj;
-            if (ids_out) ids_out[j] = e[j];
-            if (w_out) w_out[j] = wj;
-        }
+    const float ex = lane < k ? expf(my_v - v[0]) : 0.f;
+    float sum = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+        const float wj = ex / sum;
+        ids[lane] = my_e;
+        w[lane] = wj;
+        if (ids_out) ids_out[lane] = my_e;
+        if (w_out) w_out[lane] = wj;
     }
 }
 
