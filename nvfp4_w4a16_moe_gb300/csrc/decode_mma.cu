@@ -96,13 +96,6 @@ __device__ __forceinline__ WChunk load_chunk(const uint8_t* codes, const uint8_t
     return c;
 }
 
-// E4M3 block scale -> f16x2 {scale, scale} (exact).
-__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t byte) {
-    uint32_t r;
-    asm("{\n .reg .b16 b;\n cvt.u16.u32 b, %1;\n cvt.rn.f16x2.e4m3x2 %0, b;\n}" : "=r"(r) : "r"(byte * 0x101u));
-    return r;
-}
-
 // Four E2M1 code bytes (one 32-bit word: two MMA steps of one weight row) -> four
 // f16x2 of code * scale. The word is unpacked into byte registers for cvt.
 __device__ __forceinline__ void expand_word(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
@@ -121,6 +114,18 @@ __device__ __forceinline__ uint32_t word_of(const WChunk& c, int wi) {
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
+// E4M3 scales of four blocks (one 32-bit word) -> four f16x2 {scale, scale}
+// (exact): two cvt of two bytes each, then byte permutes duplicate each half.
+__device__ __forceinline__ void scales4(uint32_t sc, uint32_t (&o)[4]) {
+    uint32_t lo, hi;
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi) : "r"(sc));
+    o[0] = __byte_perm(lo, 0, 0x1010);
+    o[1] = __byte_perm(lo, 0, 0x3232);
+    o[2] = __byte_perm(hi, 0, 0x1010);
+    o[3] = __byte_perm(hi, 0, 0x3232);
+}
+
 // The 16 MMA steps of one chunk: A rows (c0: fragment rows 0-7, c1: rows 8-15),
 // B from NB staged n8 blocks (row g and g + 8 of the stage). Code word wi holds
 // steps 2wi (bytes 0, 1) and 2wi + 1 (bytes 2, 3), both in scale block wi / 2.
@@ -129,11 +134,8 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[2][4], const WChunk& c0, 
                                           const uint8_t* brow0, const uint8_t* brow1, uint32_t ubase,
                                           uint32_t xmask) {
     uint32_t s0[4], s1[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        s0[b] = e4m3_to_f16x2_dup((c0.sc >> (8 * b)) & 0xFFu);
-        s1[b] = e4m3_to_f16x2_dup((c1.sc >> (8 * b)) & 0xFFu);
-    }
+    scales4(c0.sc, s0);
+    scales4(c1.sc, s1);
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
         uint32_t a[4], u[4];
