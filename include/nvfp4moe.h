@@ -213,11 +213,15 @@ NVFP4_API nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E,
  *   k <= E <= 256, 0 <= T <= 65536.
  *   Paths: T == 1 runs the one-launch decode kernel (H % 256 == 0, H <= 2048,
  *   k*I + Is <= 8192; otherwise the multi-token path), 2 <= T <= 64 the
- *   multi-token decode kernels, T > 64 with E4M3 scales and H, I, Is multiples
- *   of 256 the grouped prefill path (tcgen05 tensor-core GEMMs with the weights
- *   expanded to bf16 in shared memory; the SwiGLU intermediate is rounded to
- *   bf16 there, the activation type). Other layers with T > 64 run as 64-token
- *   chunks of the multi-token path.
+ *   multi-token decode kernels: with E4M3 scales and H, I, Is multiples of 256
+ *   (at most 4096) four launches on the warp-level tensor cores (f16 operands:
+ *   weights expanded exactly, token rows scaled by a power of two per row so
+ *   that no value overflows f16, the SwiGLU intermediate kept in fp32 between
+ *   the passes), otherwise five launches on fp32 FMA. T > 64 with E4M3 scales
+ *   and H, I, Is multiples of 256 runs the grouped prefill path (tcgen05
+ *   tensor-core GEMMs with the weights expanded to bf16 in shared memory; the
+ *   SwiGLU intermediate is rounded to bf16 there, the activation type). Other
+ *   layers with T > 64 run as 64-token chunks of the multi-token path.
  */
 NVFP4_API nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, int32_t T, uint16_t* y,
                                int32_t* topk_ids_out, float* topk_w_out, void* workspace,
