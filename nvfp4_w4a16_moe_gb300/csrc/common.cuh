@@ -80,30 +80,6 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
     return f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
 }
 
-// E4M3 block scale -> bf16x2 of (scale * 2^112), both halves equal. The fp32
-// product is exact and has at most 4 significant bits, so its top 16 bits are
-// the bf16 value.
-__device__ __forceinline__ uint32_t e4m3_to_bf16x2_x2p112(uint32_t byte) {
-    const uint32_t b = __float_as_uint(e4m3_to_f32(byte) * 0x1p112f) >> 16;
-    return b | (b << 16);
-}
-
-// Two E2M1 codes (low byte of `byte`, low nibble first) times a block scale ->
-// bf16x2, exact. cvt gives the codes as f16; an f16 bit pattern shifted right by
-// 3 with its sign kept is a bf16 of the value times 2^-112 (the high half's low
-// three mantissa bits, which the shift moves into the low half, are zero for
-// every E2M1 value); the bf16x2 multiply by s2 = bf16x2(scale * 2^112) restores
-// the scale. Every product has at most 6 significant bits and lies in
-// [2^-10, 2688]: no step rounds.
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2_scaled(uint32_t byte, uint32_t s2) {
-    uint32_t h2;
-    asm("{\n .reg .b8 c;\n cvt.u8.u32 c, %1;\n cvt.rn.f16x2.e2m1x2 %0, c;\n}" : "=r"(h2) : "r"(byte));
-    const uint32_t b2 = ((h2 & 0x7FFF7FFFu) >> 3) | (h2 & 0x80008000u);
-    uint32_t r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(b2), "r"(s2));
-    return r;
-}
-
 // Decoded block scale of block `i` of a scale row (E4M3 bytes or FP16 halves).
 template <int KIND>
 __device__ __forceinline__ float scale_at(const void* row, int i) {

@@ -1,5 +1,8 @@
-// MoE layer, decode path (T <= 64): router GEMV, route, grouped gate/up + SiLU,
-// down + routing-weighted combine + sigmoid-gated shared expert.
+// MoE layer, multi-token decode path on fp32 FMA (T <= 64) for the layers the
+// tensor-core path in decode_mma.cu does not take (FP16 block scales, or H / I /
+// Is off the multiple-of-256 grid): router GEMV, route, grouped gate/up + SiLU,
+// down + routing-weighted combine + sigmoid-gated shared expert. This file also
+// owns the workspace layout of every T <= 64 call.
 //
 // Sources (page title, section):
 //  - lynn-engine tutorials index, row 06 "MoE router" (softmax-all -> top-k ->
