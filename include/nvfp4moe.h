@@ -235,7 +235,7 @@ NVFP4_API size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T);
  * memory budget is fixed up front). The pages have no counterpart to this call:
  * it only changes where the scratch lives.
  *   Arguments as for moe_layer_forward, without the workspace. The scratch is a
- *   static 4 MiB device array inside this library; every GPU that loads the
+ *   static 8 MiB device array inside this library; every GPU that loads the
  *   library keeps it reserved until the process exits. Nothing is allocated:
  *   no cudaMalloc, cudaFree or allocating library routine is called.
  *   The first call on a device looks up the array's device address with
@@ -244,7 +244,7 @@ NVFP4_API size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T);
  *   (an asynchronous memset on `stream`) and then runs the layer.
  *   All calls on a device share the one array: calls that can overlap on the
  *   GPU (different streams without ordering) race and must not be made.
- *   A layer whose scratch (moe_layer_workspace_size) exceeds 4 MiB is rejected
+ *   A layer whose scratch (moe_layer_workspace_size) exceeds 8 MiB is rejected
  *   with NVFP4_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. Device-side
  *   wait timeouts are recorded in the array but cannot be read back.
  */

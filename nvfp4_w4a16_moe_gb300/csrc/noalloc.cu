@@ -21,7 +21,8 @@
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = 4u << 20;   // 4 MiB per device
+constexpr size_t kNoallocScratchBytes = 8u << 20;   // 8 MiB per device (a 64-token call of a
+                                                     // 2048-wide, 256-expert, top-8 layer needs 6.0 MB)
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 

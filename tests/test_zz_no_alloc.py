@@ -28,7 +28,7 @@ def _noalloc(nv, layer, x):
     return y, ids, w
 
 
-@pytest.mark.parametrize("shape,T", [(wl.TINY, 1), (wl.TINY, 5), (wl.QWEN36_35B_A3B, 1)])
+@pytest.mark.parametrize("shape,T", [(wl.TINY, 1), (wl.TINY, 5), (wl.QWEN36_35B_A3B, 1), (wl.QWEN36_35B_A3B, 64)])
 def test_noalloc_matches_workspace_entry_point(nv, shape, T):
     L = wl.LayerInputs(shape, seed=7)
     layer = gpu_layer(L)
@@ -49,7 +49,7 @@ def test_noalloc_rejects_oversized_scratch(nv):
     layer = gpu_layer(L)
     x = torch.zeros(64, 2048, dtype=torch.bfloat16, device="cuda")
     d = layer.desc()
-    d.E, d.k, d.I, d.Is = 256, 8, 8192, 8192    # 64 tokens x 8 x 8192 intermediates: far above 4 MiB
+    d.E, d.k, d.I, d.Is = 256, 8, 8192, 8192    # 64 tokens x 8 x 8192 intermediates: far above 8 MiB
     y = torch.empty(64, 2048, dtype=torch.bfloat16, device="cuda")
     st = nv.lib.moe_layer_forward_noalloc(ctypes.byref(d), ctypes.c_void_p(x.data_ptr()), 64,
                                           ctypes.c_void_p(y.data_ptr()), None, None, nv._stream())
