@@ -30,6 +30,9 @@ WORKLOAD = ("qwen3.6-35b-a3b-shaped MoE layer decode, T=1 token/step, H=2048 E=2
             "shared Is=512 sigmoid gate, NVFP4 E4M3 per-16 scales, seeds 0..31")
 
 
+CHAIN_LAYERS = 40   # layers of the batched decode step
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -310,7 +313,9 @@ def run_batched(args, nv, wl, device):
     instances; bytes per call are the distinct active experts' weights plus the
     shared expert, the router and the activations."""
     Tb = args.tokens
-    n_inst = max(1, args.seeds)
+    # one decode step through 40 stacked layers with independent weights (18.1 GB
+    # resident): 40 layer calls in sequence on one stream, one graph replay
+    n_inst = CHAIN_LAYERS if args.seeds == N_SEEDS else max(1, args.seeds)
     layers, _ = build_layers(nv, wl, device, n_inst)
     descs = [l.desc() for l in layers]
     xb = [wl.activations(100 + i, Tb, layers[0].H, device=device) for i in range(n_inst)]
@@ -359,9 +364,16 @@ def run_batched(args, nv, wl, device):
         "dtype": "bf16-act/nvfp4-weight, bf16 MMA, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
         "config": {"workload": "qwen3.6-35b-a3b-shaped MoE layer decode, T=%d tokens per call, H=2048 E=256 "
-                               "top-8 I=512 shared Is=512, NVFP4 E4M3 per-16 scales, %d rotating instances"
-                               % (Tb, n_inst), "tokens_per_step": Tb},
+                               "top-8 I=512 shared Is=512, NVFP4 E4M3 per-16 scales, %d stacked layers with "
+                               "independent weights (%.1f GB resident)"
+                               % (Tb, n_inst, n_inst * 0.4531), "tokens_per_step": Tb,
+                   "l2": "inputs larger than L2: every layer's weights are read once per decode step"},
         "us_per_call": us, "achieved_gbs": gbs,
+        "decode_step": {"layers": n_inst, "us": us * n_inst,
+                        "note": "one graph replay = the layer calls of one decode step through the stacked "
+                                "layers, in sequence on one stream; each layer gets its own seeded input "
+                                "(the pages' layer has no norm, so a raw chain underflows within a few layers "
+                                "and would route every token to the same experts)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak if peak else None, "peak_kind": peak_kind, "traffic": None,
                      "bytes_per_launch": bytes_call,
