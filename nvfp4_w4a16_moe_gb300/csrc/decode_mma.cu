@@ -196,6 +196,14 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     const int r = blockIdx.x * kWarps + warp;
     const int t0 = blockIdx.y * kRouterTok;
     const int tc = min(kRouterTok, T - t0);
+    const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
+    uint4 wraw[8];   // this lane's chunks of the router row, requested before x is staged
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int c = lane + 32 * i;
+        wraw[i] = make_uint4(0, 0, 0, 0);
+        if (r < rows && nch <= 256 && c < nch) wraw[i] = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
+    }
     for (int i = threadIdx.x; i < tc * nch; i += kThreads)
         xs4[i] = *reinterpret_cast<const uint4*>(x + (size_t)t0 * H + 8 * (size_t)i);
     __syncthreads();
@@ -221,14 +229,11 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     if (r < rows) {
         // one token at a time (a rolled loop keeps the code small: this kernel runs
         // once per SM, so its instructions are fetched cold)
-        const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
         if (nch <= 256) {
             float wf[8][8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int c = lane + 32 * i;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (c < nch) v = *reinterpret_cast<const uint4*>(row + 8 * (size_t)c);
+                const uint4 v = wraw[i];
                 const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
@@ -296,26 +301,30 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
             }
         }
     }
-    __threadfence();
+    // barrier, then one thread fences and takes the ticket (the block's writes are
+    // ordered before the fence by the barrier)
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&hdr->route_tickets[blockIdx.y], 1u) == gridDim.x - 1;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&hdr->route_tickets[blockIdx.y], 1u) == gridDim.x - 1;
+        if (s_last) __threadfence();
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     for (int t = t0 + warp; t < t0 + tc; t += kWarps) {
         const size_t o = (size_t)t * k;
         topk_warp_mt(logits + (size_t)t * E, E, k, ids + o, w + o, ids_out ? ids_out + o : nullptr,
                           w_out ? w_out + o : nullptr);
     }
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
+        __threadfence();
         atomicExch(&hdr->route_tickets[blockIdx.y], 0u);
         s_last = atomicAdd(&hdr->route_tickets[kRouteTicketBlocks], 1u) == gridDim.y - 1;
+        if (s_last) __threadfence();
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
     if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
 }
