@@ -563,10 +563,14 @@ combine_mt_kernel(const float* __restrict__ P, const float* __restrict__ Ps, int
     const int i = blockIdx.x * kThreads + threadIdx.x;
     if (i >= T * q4) return;
     const int t = i / q4, c = i - t * q4;
+    float4 v[NVFP4_MAX_TOPK];   // all k loads in flight before the first add
+#pragma unroll
+    for (int j = 0; j < NVFP4_MAX_TOPK; ++j)
+        if (j < k) v[j] = *reinterpret_cast<const float4*>(P + (size_t)(t * k + j) * H + 4 * c);
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-        const float4 v = *reinterpret_cast<const float4*>(P + (size_t)(t * k + j) * H + 4 * c);
-        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+#pragma unroll
+    for (int j = 0; j < NVFP4_MAX_TOPK; ++j) {
+        if (j < k) { a.x += v[j].x; a.y += v[j].y; a.z += v[j].z; a.w += v[j].w; }
     }
     if (Ps) {
         const float4 v = *reinterpret_cast<const float4*>(Ps + (size_t)t * H + 4 * c);
