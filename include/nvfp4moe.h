@@ -207,8 +207,9 @@ NVFP4_API nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E,
  *   topk_ids_out  int32 [T, k] device or NULL;  topk_w_out  fp32 [T, k] or NULL
  *   workspace     >= moe_layer_workspace_size(d, T) bytes of device scratch,
  *                 zeroed once with nvfp4_workspace_init before its first use
- *                 (it carries a barrier counter across calls); calls that share
- *                 a workspace must be serialised on one stream.
+ *                 (it carries a barrier counter and the multi-token router's
+ *                 completion counters across calls); calls that share a
+ *                 workspace must be serialised on one stream.
  *   Shapes: H % 32 == 0, I % 32 == 0, Is % 32 == 0 (or Is == 0), 1 <= k <= 8,
  *   k <= E <= 256, 0 <= T <= 65536.
  *   Paths: T == 1 runs the one-launch decode kernel (H % 256 == 0, H <= 2048,
@@ -253,7 +254,9 @@ NVFP4_API nvfp4_status moe_layer_forward_noalloc(const moe_layer_desc* d, const 
                                                  void* stream);
 
 /* Zero a workspace (enqueued on `stream`). Needed once before first use, and
- * again after a call reported NVFP4_ERR_DEVICE_TIMEOUT. */
+ * again after a call reported NVFP4_ERR_DEVICE_TIMEOUT or a CUDA error (a call
+ * cut short can leave the completion counters of the multi-token router
+ * non-zero; no wait depends on them, but the next call would route wrongly). */
 NVFP4_API nvfp4_status nvfp4_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronise `stream`, then read the device status word of `workspace`
