@@ -22,7 +22,7 @@
 // Operand B is the entries' activation rows (x for gate/up, h for down), staged
 // once per CTA in shared memory as f16. Each row is first multiplied by 2^k_r, the
 // power of two that puts its largest magnitude in [2^14, 2^15): no f16 overflow
-// for any bf16 or fp32 input, and every element within 2^-28 of the row's largest
+// for any finite bf16 or fp32 row, and every element within 2^-28 of the row's largest
 // converts exactly (a bf16 has 8 significant bits, f16 11); smaller elements carry
 // an absolute error below 2^-39 of the row's largest. The epilogue multiplies the
 // fp32 accumulator by 2^-k_r (exact). Row maxima come from the router kernel (x)
@@ -62,11 +62,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // Row scaling: k with max|row| * 2^k in [2^14, 2^15), from the fp32 bits of max|row|
-// (0 for an all-zero row; clamped to [-110, 110] so that 2^k and 2^-k are normal).
+// (0 for an all-zero row; clamped to [-126, 126] so that 2^k and 2^-k are normal:
+// the largest finite row, max|row| < 2^128, still lands below 2^15).
 __device__ __forceinline__ int row_shift(uint32_t amax_bits) {
     if (amax_bits == 0u) return 0;
     const int e = (int)(amax_bits >> 23) - 127;
-    return min(110, max(-110, 14 - e));
+    return min(126, max(-126, 14 - e));
 }
 __device__ __forceinline__ float exp2i(int k) { return __int_as_float((k + 127) << 23); }
 

@@ -267,8 +267,11 @@ void orc_router_logits(const uint16_t* x, int T, int H, const uint16_t* wg, int 
         }
 }
 
-/* p = softmax over all E logits; keep the k largest p (ties: lower index first),
- * in that order; w = p_topk / sum(p_topk). probs (nullable) receives p. */
+/* p = softmax over all E logits; keep the k largest p, in that order; w =
+ * p_topk / sum(p_topk). probs (nullable) receives p. softmax is monotone in the
+ * logits, so equal p with different logits (exp underflowing to 0, or rounding
+ * to the same double) are ordered by the logits: the top-k of p as defined, not
+ * an artefact of fp64 range. Equal logits: lower index first. */
 int orc_route(const double* logits, int T, int E, int k, int32_t* ids, double* w,
               double* probs) {
     if (k < 1 || k > E) return ORC_ERR_ARG;
@@ -288,7 +291,8 @@ int orc_route(const double* logits, int T, int E, int k, int32_t* ids, double* w
             int best = -1;
             for (int e = 0; e < E; ++e) {
                 if (taken[e]) continue;
-                if (best < 0 || p[e] > p[best]) best = e;   /* strict: lower index wins ties */
+                if (best < 0 || p[e] > p[best] || (p[e] == p[best] && l[e] > l[best]))
+                    best = e;   /* strict: lower index wins exact ties */
             }
             taken[best] = 1;
             ids[(size_t)t * k + j] = best;

@@ -75,3 +75,18 @@ def test_qwen_64_tokens_deterministic(nv):
     y0 = nv.moe_layer_forward(layer, x, ws=ws)
     for _ in range(5):
         assert torch.equal(nv.moe_layer_forward(layer, x, ws=ws), y0)
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 16, 2.0 ** -16])
+def test_small_layer_activation_scale(nv, scale):
+    """Activations far from unit scale (exact power-of-two multiples of the usual
+    draw): at 2^16 a plain f16 conversion of the token rows would overflow, so this
+    checks the per-row power-of-two staging of x and h on the tensor-core path. The
+    router's fp32 logit error grows with the activations, so the logit gap below
+    which a token counts as a near tie grows with them too."""
+    L = wl.LayerInputs(SM, seed=29)
+    layer = gpu_layer(L)
+    x = (wl.activations(29, 12, SM.H).float() * scale).to(torch.bfloat16)
+    y, ids, w = _forward(nv, layer, x)
+    assert torch.isfinite(y.float()).all()
+    check_layer_parity(L, x, y, ids, w, gap_min=1e-3 * max(1.0, scale))

@@ -63,6 +63,16 @@ def test_ties_lower_index_first(orc):
     assert np.allclose(w[0, :3], w[0, 0])
 
 
+def test_underflowed_probabilities_rank_by_logits(orc):
+    """Logits 1000 apart: every p but the first underflows to 0 in fp64. softmax is
+    monotone, so the top-k of p is still the top-k of the logits."""
+    logits = np.array([[0.0, -1000.0, -2000.0, -1500.0, -3000.0]])
+    ids, w, p = orc.route(logits, 4)
+    assert np.all(p[0, 1:] == 0.0)
+    assert ids[0].tolist() == [0, 1, 3, 2]
+    assert w[0].tolist() == [1.0, 0.0, 0.0, 0.0]
+
+
 def test_route_rejects_bad_k(orc):
     with pytest.raises(ValueError):
         orc.route(np.zeros((1, 4)), 5)
