@@ -57,6 +57,21 @@ def dist_env():
     return rank, world, local
 
 
+def replicas_timing(ms_local: float, steps: int, world: int, device=None):
+    """Whole-job timing of N independent replicas: the timed region's maximum over
+    ranks (the job ends when the slowest replica does), then microseconds per token
+    over the tokens all ranks processed (each rank runs `steps` single-token steps).
+    Every rank returns the same (ms, us_per_token)."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, 1e3 * ms / (steps * world)
+
+
 def ncu_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu capture, or
     None when the kernel source changed since that capture."""
@@ -470,12 +485,7 @@ def main():
         ev1.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.2)
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
-    us_per_token = 1e3 * ms / (K * world)
+    ms, us_per_token = replicas_timing(ev0.elapsed_time(ev1), K, world, device)
     avg_bytes = sum(bytes_per_step) / n_inst
     achieved_gbs = avg_bytes / (1e3 * ms / K * 1e-6) / 1e9
 
