@@ -155,3 +155,28 @@ def test_tiny_layer_scale(orc):
     assert 1e-3 < np.abs(res.y).max() < 10
     no_sh, _ = oracle_layer(L, x, with_shared=False)
     assert not np.allclose(no_sh.y, res.y)
+
+
+def test_forced_expert_set_renormalises_over_it(orc):
+    """The tests re-evaluate near-tie tokens on the GPU's expert set: with forced
+    ids the layer must be sum_j w'_j SwiGLU_j(x) + sigmoid(gs.x) SwiGLU_s(x), w' the
+    softmax of the forced experts' logits (the renormalised probabilities)."""
+    H, I, E, k = 64, 32, 6, 2
+    x = wl.activations(9, 3, H)
+    wg = wl.normal(wl.stream_key(70), E * H, 0.4).view(E, H).to(torch.bfloat16)
+    experts = {e: _packs(orc, (H, I), 80 + e) for e in range(E)}
+    sh = _packs(orc, (H, I), 79)
+    sgv = wl.normal(wl.stream_key(71), H, 0.3).to(torch.bfloat16)
+    base = orc.moe_layer(x, wg, sgv, experts, sh, k=k)
+    forced = np.array([[e for e in range(E) if e not in base.ids[t]][:k] for t in range(3)], np.int32)
+    res = orc.moe_layer(x, wg, sgv, experts, sh, k=k, force_ids=forced)
+    logits = x.double().numpy() @ wg.double().numpy().T
+    sig = 1.0 / (1.0 + np.exp(-(x.double().numpy() @ sgv.double().numpy())))
+    shared = _dense_swiglu(orc, *sh, x)
+    for t in range(3):
+        l = logits[t, forced[t]]
+        wt = np.exp(l - l.max()) / np.exp(l - l.max()).sum()
+        want = sum(wt[j] * _dense_swiglu(orc, *experts[int(forced[t, j])], x[t:t + 1])[0] for j in range(k))
+        want = want + sig[t] * shared[t]
+        assert np.allclose(res.y[t], want, rtol=1e-11, atol=1e-15)
+        assert sorted(res.ids[t].tolist()) == sorted(forced[t].tolist())
