@@ -42,10 +42,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seeds", type=int, default=N_SEEDS, help="layer instances to rotate over")
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched", "gemv"],
                     help="decode: the single-token layer (default, the headline); prefill: one "
                          "4096-token layer call with the skewed router; batched: one --tokens-token "
-                         "decode call per step")
+                         "decode call per step; gemv: the dense W4A16 GEMV, 1 token, K=2048 -> N=8192")
     ap.add_argument("--tokens", type=int, default=64, help="tokens per call of --workload batched (1..64)")
     return ap.parse_args()
 
@@ -401,6 +401,83 @@ def run_batched(args, nv, wl, device):
     return 0
 
 
+def run_gemv(args, nv, wl, device):
+    """Dense NVFP4 W4A16 GEMV like a GatedDeltaNet in_proj_qkv: 1 token, K=2048 -> N=8192,
+    FP16 block scales (the value) and E4M3 block scales (reported beside). 16 packed
+    weight instances (168 MB) rotate so that every call reads cold weights; one CUDA
+    graph replays a pass over them. Bytes per call: codes, scales, tensor scale, x, y."""
+    N, K, T = 8192, 2048, 1
+    n_inst = 16
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    res = {}
+    clk_summary = None
+    for kind, name in ((nv.SCALE_FP16, "fp16"), (nv.SCALE_E4M3, "e4m3")):
+        Ws = []
+        for i in range(n_inst):
+            w = wl.dense_weight_f32(1 + i, N, K, device=device)
+            Ws.append(nv.nvfp4_pack(w, kind))
+            del w
+        xs = [wl.activations(1 + i, T, K, device=device) for i in range(n_inst)]
+        ys = [torch.empty(T, N, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
+        sb = 2 if kind == nv.SCALE_FP16 else 1
+        bytes_call = N * K // 2 + N * (K // 16) * sb + 4 + 2 * K * T + 2 * N * T
+        cap = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            for i in range(n_inst):
+                nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(n_inst):
+                    nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])
+        torch.cuda.synchronize()
+        W = max(3, args.warmup)
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        passes = max(1, -(-max(1, args.steps) // n_inst))
+        K_calls = passes * n_inst
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(device.index or 0) as clk:
+            time.sleep(0.3)
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for _ in range(passes):
+                g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            time.sleep(0.2)
+        us = 1e3 * ev0.elapsed_time(ev1) / K_calls
+        gbs = bytes_call / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": us, "bytes_per_call": bytes_call, "achieved_gbs": gbs,
+                     "frac_of_hbm_peak": gbs / peak if peak else None, "calls": K_calls}
+        if kind == nv.SCALE_FP16:
+            clk_summary = clk.summary()
+        del Ws, xs, ys, g
+    f = res["fp16"]
+    line = {
+        "metric": "NVFP4 dense W4A16 GEMV, 1 token, K=2048 -> N=8192: us per call and achieved HBM GB/s",
+        "value": f["us_per_call"], "unit": "us/call", "n_gpus": 1, "steps": f["calls"], "warmup": max(3, args.warmup),
+        "ms_per_step": f["us_per_call"] * 1e-3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-act/nvfp4-weight, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
+        "config": {"workload": "dense NVFP4 W4A16 GEMV (GatedDeltaNet in_proj_qkv shape), T=1, K=2048, N=8192, "
+                               "FP16 per-16 scales; 16 rotating weight instances (168 MB)", "tokens_per_step": 1,
+                   "l2": "inputs larger than L2: 16 rotating instances"},
+        "roofline": {"bound": "hbm", "achieved": f["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": f["frac_of_hbm_peak"], "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": f["bytes_per_call"], "kernel": "gemv_kernel (one launch per call)"},
+        "e4m3": res["e4m3"],
+        "gpu_launches": f["calls"],
+        "clocks": clk_summary,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -424,6 +501,10 @@ def main():
         if world > 1 and rank != 0:
             return 0
         return run_batched(args, nv, wl, device)
+    if args.workload == "gemv":
+        if world > 1 and rank != 0:
+            return 0
+        return run_gemv(args, nv, wl, device)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
