@@ -167,10 +167,19 @@ NVFP4_API size_t nvfp4_pack_workspace_size(void);
  *   Defined by: Lynn Engine write-up, "P1 stage" (packed matvec computed from
  *   E2M1 + per-16 scale without a bf16 copy); lynn-engine README, P1-A
  *   (batched M > 1 packed projections).
- *   W   NVFP4 matrix (K % 32 == 0, 1 <= N, K <= 65536), either scale kind
- *   x   bf16 [T, K] device;  y  bf16 [T, N] device (written; fp32 accumulation,
- *       one rounding to bf16)
- *   workspace may be NULL with 0 bytes (this call needs none).
+ *   W   NVFP4 matrix (K % 32 == 0, 32 <= K <= 8192, 1 <= N <= 2^22), either
+ *       scale kind
+ *   x   bf16 [T, K] device;  y  bf16 [T, N] device (written; exact products,
+ *       fp32 accumulation, one rounding to bf16)
+ *   workspace  NULL (0 bytes), or >= 256 bytes of device memory zeroed with
+ *       nvfp4_workspace_init: the call needs no scratch, but a bounded device
+ *       wait that ran out is then recorded in its status word. Such a wait also
+ *       writes quiet-NaN bf16 into the affected rows of y.
+ *   Up to 8 tokens share one pass over the weights; T > 8 streams them
+ *   ceil(T/8) times. The weights are requested before the kernel waits for the
+ *   previous kernel on the stream (programmatic dependent launch), so they must
+ *   not be written by a kernel that is still running; nvfp4_pack makes its
+ *   output visible before it completes.
  */
 NVFP4_API nvfp4_status nvfp4_gemv_w4a16(const nvfp4_weight* W, const uint16_t* x, int32_t T, uint16_t* y,
                               void* workspace, size_t workspace_bytes, void* stream);

@@ -112,16 +112,16 @@ nvfp4_status nvfp4_pack(const float* w, int32_t N, int32_t K, int32_t kind, uint
 
 nvfp4_status nvfp4_gemv_w4a16(const nvfp4_weight* W, const uint16_t* x, int32_t T, uint16_t* y,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     nvfp4_status st = check_weight(W);
     if (st != NVFP4_OK) return st;
     if (!x || !y) return NVFP4_ERR_INVALID_ARG;
     if (T < 1 || T > NVFP4_MAX_GEMV_TOKENS) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned16(x) || !aligned16(y)) return NVFP4_ERR_MISALIGNED;
+    if (!aligned16(x) || !aligned16(y) || (workspace && !aligned16(workspace))) return NVFP4_ERR_MISALIGNED;
+    if (workspace && workspace_bytes < sizeof(WsHeader)) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     DeviceInfo dev;
     if ((st = device_info(&dev)) != NVFP4_OK) return st;
-    return from_cuda(launch_gemv(*W, x, T, y, dev, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemv(*W, x, T, y, static_cast<WsHeader*>(workspace), dev, g_wait_limit.load(),
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 nvfp4_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,

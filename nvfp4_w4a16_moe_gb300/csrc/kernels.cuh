@@ -16,8 +16,9 @@ struct DeviceInfo {
 cudaError_t launch_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scales,
                         float* tensor_scale, WsHeader* ws, int num_sms, cudaStream_t s);
 
-cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_t* y,
-                        const DeviceInfo& dev, cudaStream_t s);
+// hdr (nullable): where a bounded wait that ran out is recorded
+cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_t* y, WsHeader* hdr,
+                        const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                               cudaStream_t s);

@@ -60,7 +60,10 @@ __global__ void pack_quant_kernel(const float* __restrict__ w, size_t nblocks,
     float s_t = 1.0f;
     if (KIND == NVFP4_SCALE_E4M3 && amax_t > 0.0f) s_t = __fdiv_rn(amax_t, 2688.0f);
     const size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-    if (b == 0) *tensor_scale = s_t;
+    if (b == 0) {
+        *tensor_scale = s_t;
+        __threadfence();
+    }
     if (b >= nblocks) return;
     const float4* src = reinterpret_cast<const float4*>(w + b * 16);
     float v[16];
@@ -97,6 +100,11 @@ __global__ void pack_quant_kernel(const float* __restrict__ w, size_t nblocks,
         }
     }
     *reinterpret_cast<uint2*>(packed + b * 8) = make_uint2(out[0], out[1]);
+    // The layer and GEMV kernels launch with programmatic stream serialisation and
+    // request their weights before griddepcontrol.wait; a packer that wrote those
+    // weights right before them on the same stream has its bytes visible at GPU scope
+    // before it completes.
+    __threadfence();
 }
 
 cudaError_t launch_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scales,
