@@ -253,3 +253,121 @@ def logit_gap(logits, k: int) -> np.ndarray:
     if lg.shape[1] <= k:
         return np.full(lg.shape[0], np.inf)
     return lg[:, k - 1] - lg[:, k]
+
+
+# ------------------------------------------------------- the layer for many tokens
+#
+# The same layer as moe_layer, evaluated expert by expert so that thousands of
+# tokens take seconds instead of hours. Nothing is approximated: the dequantised
+# matrices are the exact products code x block scale x tensor scale (fp64), each
+# expert's SwiGLU is the definition written with numpy's fp64 matmul as the
+# library step, and every token's output sums its k weighted expert rows in rank
+# order, then the gated shared row, as moe_layer does (tutorials index, row 06;
+# README P28/P29 notes). Pinned against moe_layer in tests/test_oracle_batched.py.
+
+_TABLES = {}
+
+
+def _decode_tables(kind: int):
+    """E2M1 values of the 16 codes and the values of every scale code, from the C decoders."""
+    t = _TABLES.get(kind)
+    if t is None:
+        e2m1 = np.array([e2m1_decode(c) for c in range(16)], np.float64)
+        if kind == SCALE_E4M3:
+            sc = np.array([e4m3_decode(b) for b in range(256)], np.float64)
+        else:
+            sc = np.array([fp16_decode(b) for b in range(65536)], np.float64)
+        t = (e2m1, sc)
+        _TABLES[kind] = t
+    return t
+
+
+def dequant_table(p: Packed) -> np.ndarray:
+    """dequant(p) by table lookup: W[n, k] = E2M1(code) * scale(n, k // 16) * tensor_scale."""
+    e2m1, sc = _decode_tables(p.kind)
+    codes = np.empty((p.N, p.K), np.uint8)
+    codes[:, 0::2] = p.packed & 15
+    codes[:, 1::2] = p.packed >> 4
+    s = np.repeat(sc[p.scales.astype(np.int64)], 16, axis=1)
+    return e2m1[codes] * s * float(p.tensor_scale)
+
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def bf16_rows(x) -> np.ndarray:
+    """bf16 [T, H] (torch tensor or uint16 bits) -> exact fp64 values."""
+    xb = _np(x, np.uint16)
+    return (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def swiglu_rows(g: Packed, u: Packed, d: Packed, xrows: np.ndarray) -> np.ndarray:
+    """D (silu(G x) * (U x)) for every row x of xrows (fp64 [n, H]) -> fp64 [n, H]."""
+    if xrows.shape[0] == 0:
+        return np.zeros((0, d.N), np.float64)
+    G, U, D = dequant_table(g), dequant_table(u), dequant_table(d)
+    h = _silu(xrows @ G.T) * (xrows @ U.T)
+    return h @ D.T
+
+
+def route_tokens(x, router_w, k: int, force_ids=None):
+    """(logits, ids, w, p) of moe_layer's router; with force_ids the weights are p over the
+    forced set, renormalised (as moe_layer does for near-tie tokens)."""
+    logits = router_logits(x, router_w)
+    ids, w, p = route(logits, k)
+    if force_ids is not None:
+        ids = _np(force_ids, np.int32).copy()
+        w = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+        w = w / w.sum(axis=1, keepdims=True)
+    return logits, ids, w, p
+
+
+def shared_gate(x, sh_gate_vec) -> np.ndarray:
+    """sigmoid(gs . x) per token (fp64)."""
+    z = bf16_rows(x) @ bf16_rows(_np(sh_gate_vec, np.uint16)[None, :])[0]
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def combine(rows: np.ndarray, w: np.ndarray, shared_rows=None, sig=None) -> np.ndarray:
+    """y[t] = sum_j w[t, j] rows[t, j] (j in rank order) + sig[t] * shared_rows[t]."""
+    T, k, H = rows.shape
+    y = np.zeros((T, H), np.float64)
+    for j in range(k):
+        y += w[:, j:j + 1] * rows[:, j, :]
+    if shared_rows is not None:
+        y += sig[:, None] * shared_rows
+    return y
+
+
+def moe_layer_batched(x, router_w, sh_gate_vec, experts: dict, shared, k: int, force_ids=None,
+                      expert_rows=None, routing=None) -> LayerResult:
+    """moe_layer for many tokens. ``experts`` maps expert id -> (gate, up, down) Packed (only the
+    routed ones are needed). ``expert_rows(e, token_indices) -> fp64 [n, H]`` may replace the
+    per-expert evaluation (the tests run it in worker processes); by default it is
+    swiglu_rows on ``experts[e]``. ``routing`` = (ids, w) from route_tokens with the same
+    arguments skips recomputing the router."""
+    xr = bf16_rows(x)
+    T = xr.shape[0]
+    if routing is None:
+        _, ids, w, _ = route_tokens(x, router_w, k, force_ids)
+    else:
+        ids, w = routing
+    H = xr.shape[1]
+    rows = np.zeros((T, k, H), np.float64)
+    for e in np.unique(ids):
+        tt, jj = np.nonzero(ids == e)
+        if expert_rows is not None:
+            out = expert_rows(int(e), tt)
+        else:
+            if int(e) not in experts:
+                raise KeyError("routing selected an expert that was not provided")
+            out = swiglu_rows(*experts[int(e)], xr[tt])
+        rows[tt, jj] = out
+    sig = np.zeros(T, np.float64)
+    srows = None
+    if shared is not None:
+        sig = shared_gate(x, sh_gate_vec)
+        srows = swiglu_rows(*shared, xr)
+    y = combine(rows, w, srows, sig if shared is not None else None)
+    return LayerResult(y, ids, w, sig)

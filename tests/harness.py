@@ -116,3 +116,120 @@ def check_layer_parity(L: wl.LayerInputs, x_gpu, y_gpu, ids_gpu, w_gpu, kind=0, 
         ok2, err2, bound2 = tol_ok(got, ref, rel=rel_only, abs_=0.0)
         assert ok2, "max|gpu-oracle| %.4g > %.4g (scale-free)" % (err2, bound2)
     return err, bound, int(near.sum())
+
+
+# ------------------------------------------------------------------------------------
+# The oracle at full size: every token of a call, with the routed experts evaluated in
+# worker processes (oracle.moe_layer_batched with its expert_rows hook). Workers are
+# started with "spawn" (never forked from a process that holds a CUDA context), one
+# BLAS / OpenMP thread each.
+
+_POOL = None
+_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def _worker_init():
+    torch.set_num_threads(1)
+
+
+def oracle_pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        import os
+        for k in _THREAD_ENV:
+            os.environ[k] = "1"     # read by the workers' numpy / torch at import
+        n = max(1, min(48, os.cpu_count() or 1))
+        _POOL = cf.ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"),
+                                       initializer=_worker_init)
+    return _POOL
+
+
+def _expert_rows_task(shape, seed, layer, kind, e, xbits):
+    """SwiGLU rows of routed expert e (redrawn from its seed, packed by the oracle) for the
+    given bf16 token rows."""
+    L = wl.LayerInputs(shape, seed=seed, layer=layer)
+    packs = [oracle.pack(m, kind) for m in L.expert_f32(e, device="cpu")]
+    return oracle.swiglu_rows(*packs, oracle.bf16_rows(xbits))
+
+
+class OracleJob:
+    """One oracle layer evaluation of x (bf16 [T, H]) on layer L, its experts submitted to
+    the worker pool at construction; result() assembles the layer."""
+
+    def __init__(self, L: wl.LayerInputs, x, kind=oracle.SCALE_E4M3, force_ids=None, with_shared=True,
+                 logits=None):
+        self.L, self.kind, self.with_shared = L, kind, with_shared
+        self.x = x
+        self.wg = L.router_w("cpu")
+        if logits is None:
+            logits = oracle.router_logits(x, self.wg)
+        self.logits = logits
+        ids, w, p = oracle.route(logits, L.shape.k)
+        if force_ids is not None:
+            ids = np.asarray(force_ids, np.int32).copy()
+            w = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+            w = w / w.sum(axis=1, keepdims=True)
+        self.ids, self.w = ids, w
+        xb = oracle._np(x, np.uint16)
+        pool = oracle_pool()
+        self.fut = {}
+        for e in np.unique(ids):
+            tt, _ = np.nonzero(ids == e)
+            self.fut[int(e)] = pool.submit(_expert_rows_task, L.shape, L.seed, L.layer, kind, int(e), xb[tt])
+
+    def result(self) -> oracle.LayerResult:
+        shared = oracle_shared(self.L, self.kind) if self.with_shared else None
+
+        def rows(e, tt):
+            r = self.fut[e].result()
+            assert r.shape[0] == len(tt)
+            return r
+        return oracle.moe_layer_batched(self.x, self.wg, self.L.shared_sigmoid_w("cpu"), {}, shared,
+                                        self.L.shape.k, expert_rows=rows, routing=(self.ids, self.w))
+
+
+class ParityCheck:
+    """check_layer_parity for every token of a large call, with the oracle in the worker pool.
+    Construction submits the work (so that many layers can be in flight at once); check()
+    asserts the same bar as check_layer_parity and returns (err, bound, n_near_ties)."""
+
+    def __init__(self, L: wl.LayerInputs, x_gpu, y_gpu, ids_gpu, w_gpu, kind=0, with_shared=True,
+                 gap_min=1e-3, rel_only=None):
+        self.x = x_gpu.cpu()
+        self.y = y_gpu.float().cpu().numpy().astype(np.float64)
+        self.ids_g = ids_gpu.cpu().numpy()
+        self.w_g = w_gpu.cpu().numpy()
+        self.rel_only = rel_only
+        self.job = OracleJob(L, self.x, kind, with_shared=with_shared)
+        gap = oracle.logit_gap(self.job.logits, L.shape.k)
+        self.near = np.flatnonzero(gap <= gap_min)
+        self.job_near = None
+        if self.near.size:
+            idx = torch.tensor(self.near, dtype=torch.long)
+            self.job_near = OracleJob(L, self.x[idx], kind, force_ids=self.ids_g[self.near],
+                                      with_shared=with_shared, logits=self.job.logits[self.near])
+
+    def check(self):
+        res = self.job.result()
+        clear = np.ones(len(self.ids_g), bool)
+        clear[self.near] = False
+        ids_o = res.ids
+        assert np.array_equal(np.sort(self.ids_g[clear], 1), np.sort(ids_o[clear], 1)), "expert ids differ"
+        # weights by expert id: sort both sides by id
+        og = np.argsort(self.ids_g, 1, kind="stable")
+        oo = np.argsort(ids_o, 1, kind="stable")
+        wg = np.take_along_axis(self.w_g, og, 1)[clear]
+        wo = np.take_along_axis(res.w, oo, 1)[clear]
+        if wg.size:
+            assert float(np.abs(wg - wo).max()) <= 1e-5, float(np.abs(wg - wo).max())
+        ref = res.y.copy()
+        if self.job_near is not None:
+            ref[self.near] = self.job_near.result().y
+        ok, err, bound = tol_ok(self.y, ref)
+        assert ok, "max|gpu-oracle| %.4g > %.4g" % (err, bound)
+        if self.rel_only is not None:
+            ok2, err2, bound2 = tol_ok(self.y, ref, rel=self.rel_only, abs_=0.0)
+            assert ok2, "max|gpu-oracle| %.4g > %.4g (scale-free)" % (err2, bound2)
+        return err, bound, int(self.near.size)

@@ -180,3 +180,19 @@ def test_forced_expert_set_renormalises_over_it(orc):
         want = want + sig[t] * shared[t]
         assert np.allclose(res.y[t], want, rtol=1e-11, atol=1e-15)
         assert sorted(res.ids[t].tolist()) == sorted(forced[t].tolist())
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_orc_swiglu_equals_dense_swiglu(orc, kind):
+    """The oracle's single-expert entry point (bf16 tokens in, fp64 out) is the textbook
+    SwiGLU on the dequantised matrices, token by token."""
+    H, I = 96, 64
+    g, u, d = _packs(orc, (H, I), 40 + kind, kind)
+    x = wl.activations(40 + kind, 4, H)
+    got = orc.swiglu(g, u, d, x)
+    want = _dense_swiglu(orc, g, u, d, x)
+    assert got.shape == (4, H)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
+    # one token at a time gives the same rows
+    for t in range(4):
+        assert np.array_equal(orc.swiglu(g, u, d, x[t:t + 1])[0], got[t])

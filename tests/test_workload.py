@@ -64,3 +64,12 @@ def test_layer_inputs_shapes():
     assert x.shape == (3, 256) and x.dtype == torch.bfloat16
     x2 = wl.activations(0, 3, 256, attempts=[0, 1, 0])
     assert torch.equal(x[0], x2[0]) and not torch.equal(x[1], x2[1])
+
+
+def test_cpu_and_torch_draws_are_bit_identical():
+    """The CPU path (numpy uint64) and the torch int64 path draw the same bits."""
+    for key, n, std, start in [(wl.stream_key(1, 2, 3), 100003, 0.02, 0), (wl.stream_key(5), 4097, 1.0, 1),
+                               (0xFFFFFFFF, 1000, 0.5, (1 << 31) - 7), (0, 33, 3.0, 12)]:
+        a = wl.normal(key, n, std, "cpu", start)
+        b = wl._normal_torch(key, n, std, "cpu", start)
+        assert a.dtype == torch.float32 and torch.equal(a, b)
