@@ -40,13 +40,16 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--seeds", type=int, default=N_SEEDS, help="layer instances to rotate over")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched", "gemv"],
                     help="decode: the single-token layer (default, the headline); prefill: one "
                          "4096-token layer call with the skewed router; batched: one --tokens-token "
                          "decode call per step; gemv: the dense W4A16 GEMV, 1 token, K=2048 -> N=8192")
     ap.add_argument("--tokens", type=int, default=64, help="tokens per call of --workload batched (1..64)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload: time only the single-token steps (skip the batched, 40-layer, "
+                         "GEMV and prefill figures)")
     return ap.parse_args()
 
 
@@ -151,48 +154,71 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------ oracle arm
 
-def cpu_oracle_sample(budget_s: float, max_tokens: int = 64):
-    """Time the CPU oracle on single tokens of the same workload (weights packed
-    beforehand, as the GPU's are). Returns (us_per_token, tokens, cores)."""
+def _oracle_token_inputs(seed):
+    """Everything the oracle needs for one single-token step of layer instance ``seed``
+    (the experts its router picks, packed beforehand as the GPU's weights are)."""
     import oracle
     import workload as wl
-    import numpy as np
     shape = wl.QWEN36_35B_A3B
-    times = []
-    t_start = time.time()
-    seed = 0
-    while len(times) < max_tokens and (time.time() - t_start) < budget_s:
-        L = wl.LayerInputs(shape, seed=seed % N_SEEDS)
-        x = wl.activations(seed % N_SEEDS, 1, shape.H)
-        wg = L.router_w("cpu")
-        ids, _, _ = oracle.route(oracle.router_logits(x, wg), shape.k)
-        experts = {}
-        for e in ids.ravel().tolist():
-            g, u, d = L.expert_f32(e)
-            experts[e] = (oracle.pack(g), oracle.pack(u), oracle.pack(d))
-        sg, su, sd = L.shared_f32()
-        shared = (oracle.pack(sg), oracle.pack(su), oracle.pack(sd))
-        sgv = L.shared_sigmoid_w("cpu")
+    L = wl.LayerInputs(shape, seed=seed % N_SEEDS)
+    x = wl.activations(seed % N_SEEDS, 1, shape.H)
+    wg = L.router_w("cpu")
+    ids, _, _ = oracle.route(oracle.router_logits(x, wg), shape.k)
+    experts = {e: tuple(oracle.pack(m) for m in L.expert_f32(e)) for e in ids.ravel().tolist()}
+    shared = tuple(oracle.pack(m) for m in L.shared_f32())
+    return x, wg, L.shared_sigmoid_w("cpu"), experts, shared, shape.k
+
+
+def cpu_oracle_sample(budget_s: float, threads: int = 1, max_tokens: int = 64):
+    """Time the CPU oracle on single-token steps of the same workload, one token per layer
+    instance (seeds 0..31 in turn). threads = 1: tokens one after another, ~budget_s of
+    oracle time. threads > 1: 2 * threads tokens run concurrently on that many host threads
+    (each a plain oracle call; ctypes releases the GIL), timed by the wall clock.
+    Returns (us_per_token, tokens, seconds)."""
+    import concurrent.futures as cf
+    import oracle
+    if threads <= 1:
+        times, t_start, seed = [], time.time(), 0
+        while len(times) < max_tokens and (time.time() - t_start) < budget_s:
+            inp = _oracle_token_inputs(seed)
+            t0 = time.perf_counter()
+            oracle.moe_layer(*inp)
+            times.append(time.perf_counter() - t0)
+            seed += 1
+        return 1e6 * sum(times) / len(times), len(times), sum(times)
+    n = 2 * threads
+    with cf.ThreadPoolExecutor(threads) as ex:
+        inputs = list(ex.map(_oracle_token_inputs, range(n)))
         t0 = time.perf_counter()
-        oracle.moe_layer(x, wg, sgv, experts, shared, shape.k)
-        times.append(time.perf_counter() - t0)
-        seed += 1
-    us = 1e6 * sum(times) / len(times)
-    return us, len(times), sum(times)
+        list(ex.map(lambda a: oracle.moe_layer(*a), inputs))
+        wall = time.perf_counter() - t0
+    return 1e6 * wall / n, n, wall
+
+
+def cpu_baseline_block(budget_s: float):
+    """The oracle timed on the host: all cores (the reported value) and one thread."""
+    cores = os.cpu_count() or 1
+    us1, n1, t1 = cpu_oracle_sample(budget_s, 1)
+    usn, nn, tn = cpu_oracle_sample(budget_s, cores)
+    return {"value": usn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d single-token layer calls (one per layer instance, seeds 0..%d) on %d host threads, "
+                      "%.1f s wall" % (nn, min(nn, N_SEEDS) - 1, cores, tn),
+            "single_thread": {"value": us1, "unit": UNIT, "cores": 1,
+                              "sample": "%d single-token layer calls one after another, %.1f s" % (n1, t1)}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    us, n, tot = cpu_oracle_sample(max(5.0, args.cpu_seconds))
+    cpu = cpu_baseline_block(max(5.0, args.cpu_seconds))
+    us = cpu["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": n, "warmup": 0, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "steps": int(cpu["sample"].split()[0]), "warmup": 0, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": "%d single-token layer calls" % n},
-        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "%d tokens of the T=1 decode workload (seeds 0..%d), %.1f s of CPU" %
-                                   (n, min(n, N_SEEDS) - 1, tot)},
+        "config": {"workload": WORKLOAD, "sample": cpu["sample"]},
+        "cpu_baseline": cpu,
+        "tokens_per_s": 1e6 / us,
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -240,10 +266,10 @@ def prefill_flops(shape, T, has_shared=True):
     return f
 
 
-def run_prefill(args, nv, wl, device):
+def measure_prefill(nv, wl, device, steps, warmup):
     """One 4096-token call of the Qwen3.6-35B-A3B-shaped layer per step, router rows
     scaled by rank^-kappa (kappa from the committed calibration) so that per-expert
-    token counts range from about 20 to 1000."""
+    token counts range from about 20 to 1000. Returns the measured figures."""
     import dataclasses
     gold = json.load(open(PREFILL_GOLDEN))
     shape = dataclasses.replace(wl.QWEN36_35B_A3B, router_kappa=gold["kappa"])
@@ -259,10 +285,10 @@ def run_prefill(args, nv, wl, device):
     ws = nv.Workspace(nv.moe_layer_workspace_size(layer, T), device=device)
     y = torch.empty(T, shape.H, dtype=torch.bfloat16, device=device)
     stream = torch.cuda.current_stream()
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         nv.moe_layer_forward(layer, x, ws=ws, y=y, desc=d)
     torch.cuda.synchronize()
-    K = max(1, args.steps)
+    K = max(1, steps)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index or 0) as clk:
@@ -295,171 +321,195 @@ def run_prefill(args, nv, wl, device):
     mp = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak, kind = (json.load(open(mp)).get("bf16_tflops_sustained"), "measured (sustained)") if os.path.exists(mp) \
         else (1700.0, "fallback (sustained)")
+    res = {"us_per_call": 1e3 * ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops, "peak_tflops": peak,
+           "peak_kind": kind, "frac_of_bf16_peak": tflops / peak if peak else None, "flops_per_call": flops,
+           "e2e_us_per_call": 1e3 * e2e_ms, "calls": K, "tokens": T, "kappa": gold["kappa"],
+           "entries_per_expert": [gold["min_count"], gold["max_count"]], "clocks": clk.summary(),
+           "launches_per_call": nv.launches_per_layer_call(T, shape.H)}
+    del layer, ws, x, y
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill(args, nv, wl, device):
+    r = measure_prefill(nv, wl, device, args.steps, args.warmup)
+    T = r["tokens"]
     line = {
-        "metric": "NVFP4 MoE-layer prefill: us per 4096-token layer call", "value": 1e3 * ms, "unit": "us/call",
-        "n_gpus": 1, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": False,
+        "metric": "NVFP4 MoE-layer prefill: us per 4096-token layer call", "value": r["us_per_call"],
+        "unit": "us/call", "n_gpus": 1, "steps": r["calls"], "warmup": max(3, args.warmup),
+        "ms_per_step": r["us_per_call"] * 1e-3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16-act/nvfp4-weight, bf16 MMA, f32 accumulate",
-        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16, router rows scaled by rank^-%g)"
-                % gold["kappa"],
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16, router rows scaled by "
+                "rank^-%g)" % r["kappa"],
         "config": {"workload": "qwen3.6-35b-a3b-shaped MoE layer prefill, T=%d tokens, H=2048 E=256 top-8 I=512 "
-                               "Is=512, skewed router (per-expert entries %d..%d), seed %d"
-                               % (T, gold["min_count"], gold["max_count"], seed),
-                   "tokens_per_step": T,
-                   "l2": "inputs larger than L2 (453 MB of NVFP4 weights per call)"},
-        "tokens_per_s": T / (ms * 1e-3),
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak if peak else None, "peak_kind": kind, "traffic": None,
-                     "flops_per_launch": flops,
+                               "Is=512, skewed router (per-expert entries %d..%d), seed 2"
+                               % (T, r["entries_per_expert"][0], r["entries_per_expert"][1]),
+                   "tokens_per_step": T, "l2": "inputs larger than L2 (453 MB of NVFP4 weights per call)"},
+        "tokens_per_s": r["tokens_per_s"],
+        "roofline": {"bound": "tensor", "achieved": r["tflops"], "peak": r["peak_tflops"], "unit": "TFLOP/s",
+                     "frac": r["frac_of_bf16_peak"], "peak_kind": r["peak_kind"], "traffic": None,
+                     "flops_per_launch": r["flops_per_call"],
                      "kernel": "whole step (router GEMM, top-k, expert lists, grouped tcgen05 gate/up and down "
                                "GEMMs, combine): algorithmic FLOPs / step time"},
-        "e2e": {"value": 1e3 * e2e_ms, "unit": "us/call", "h2d_bytes_per_step": 2 * T * shape.H,
-                "d2h_bytes_per_step": 2 * T * shape.H},
-        "gpu_launches": nv.launches_per_layer_call(T, shape.H) * K,
-        "clocks": clk.summary(),
+        "e2e": {"value": r["e2e_us_per_call"], "unit": "us/call", "h2d_bytes_per_step": 2 * T * 2048,
+                "d2h_bytes_per_step": 2 * T * 2048},
+        "gpu_launches": r["launches_per_call"] * r["calls"],
+        "clocks": r["clocks"],
         "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_batched(args, nv, wl, device):
-    """One decode call of --tokens tokens per step through --seeds rotating layer
-    instances (the multi-token kernels), CUDA-graph replayed in passes over the
-    instances; bytes per call are the distinct active experts' weights plus the
-    shared expert, the router and the activations."""
-    Tb = args.tokens
-    # one decode step through 40 stacked layers with independent weights (18.1 GB
-    # resident): 40 layer calls in sequence on one stream, one graph replay
-    n_inst = CHAIN_LAYERS if args.seeds == N_SEEDS else max(1, args.seeds)
-    layers, _ = build_layers(nv, wl, device, n_inst)
-    descs = [l.desc() for l in layers]
-    xb = [wl.activations(100 + i, Tb, layers[0].H, device=device) for i in range(n_inst)]
-    yb = [torch.empty(Tb, layers[0].H, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
+def graph_of(calls, cap_stream):
+    """Capture the given zero-argument launches once as one CUDA graph (after one eager
+    pass, which also warms the library's per-device state)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap_stream):
+        for c in calls:
+            c()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap_stream):
+            for c in calls:
+                c()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, reps, stream, device=None, clocks=False):
+    """Device time (ms) of `reps` back-to-back replays, CUDA events on the launching stream."""
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(device.index or 0) if clocks else None
+    if clk:
+        clk.__enter__()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if clk:
+        time.sleep(0.2)
+        clk.__exit__()
+    return ev0.elapsed_time(ev1), (clk.summary() if clk else None)
+
+
+def measure_batched(nv, wl, device, layers, descs, Tb, rotate, stream, reps=None):
+    """Decode calls of Tb tokens. rotate=True: one call per step over the layer instances
+    (graph passes), the per-call figure; rotate=False: one decode step through all the
+    stacked layers (each with its own seeded input), the per-step figure."""
+    n_inst = len(layers)
+    H = layers[0].H
+    xb = [wl.activations(100 + i, Tb, H, device=device) for i in range(n_inst)]
+    yb = [torch.empty(Tb, H, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
     ws = nv.Workspace(nv.moe_layer_workspace_size(layers[0], Tb), device=device)
     ids = []
     for i in range(n_inst):
         _, ids_i, _ = nv.moe_layer_forward(layers[i], xb[i], ws=ws, want_route=True, desc=descs[i])
         ids.append(ids_i.cpu().numpy().ravel())
     bytes_call = sum(step_bytes(layers[i], ids[i], T=Tb) for i in range(n_inst)) / n_inst
-    stream = torch.cuda.current_stream()
-    cap = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        for i in range(n_inst):
-            nv.moe_layer_forward(layers[i], xb[i], ws=ws, y=yb[i], desc=descs[i])
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(n_inst):
-                nv.moe_layer_forward(layers[i], xb[i], ws=ws, y=yb[i], desc=descs[i])
-    torch.cuda.synchronize()
-    W = max(3, args.warmup)
-    for _ in range(-(-W // n_inst)):
+    cap = torch.cuda.Stream(device=device)
+    calls = [(lambda i=i: nv.moe_layer_forward(layers[i], xb[i], ws=ws, y=yb[i], desc=descs[i]))
+             for i in range(n_inst)]
+    g = graph_of(calls, cap)
+    for _ in range(3):
         g.replay()
-    torch.cuda.synchronize()
-    passes = max(1, -(-max(1, args.steps) // n_inst))
-    K = passes * n_inst
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index or 0) as clk:
-        time.sleep(0.3)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(passes):
-            g.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        time.sleep(0.2)
-    us = 1e3 * ev0.elapsed_time(ev1) / K
-    gbs = bytes_call / (us * 1e-6) / 1e9
+    reps = reps or max(1, 256 // n_inst)
+    ms, _ = time_graph(g, reps, stream)
+    us_call = 1e3 * ms / (reps * n_inst)
+    peak, _ = measured_peaks()
+    gbs = bytes_call / (us_call * 1e-6) / 1e9
+    out = {"tokens": Tb, "us_per_call": us_call, "us_per_token": us_call / Tb, "tokens_per_s": 1e6 * Tb / us_call,
+           "bytes_per_call": bytes_call, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak if peak else None,
+           "launches_per_call": nv.launches_per_layer_call(Tb, H)}
+    if not rotate:
+        out = {"tokens": Tb, "layers": n_inst, "ms_per_decode_step": us_call * n_inst / 1e3,
+               "us_per_layer_call": us_call, "tokens_per_s": 1e6 * Tb / (us_call * n_inst),
+               "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak if peak else None,
+               "bytes_per_layer_call": bytes_call}
+    del ws, xb, yb, g
+    return out
+
+
+def run_batched(args, nv, wl, device):
+    """One decode step of --tokens tokens through 40 stacked layers with independent
+    weights (18.1 GB resident): the 40 layer calls in sequence on one stream, graph
+    replayed; bytes per call are the distinct active experts' weights plus the shared
+    expert, the router and the activations."""
+    Tb = args.tokens
+    n_inst = CHAIN_LAYERS if args.seeds == N_SEEDS else max(1, args.seeds)
+    layers, _ = build_layers(nv, wl, device, n_inst)
+    descs = [l.desc() for l in layers]
+    stream = torch.cuda.current_stream()
+    reps = max(1, -(-max(1, args.steps) // n_inst))
+    r = measure_batched(nv, wl, device, layers, descs, Tb, False, stream, reps=reps)
     peak, peak_kind = measured_peaks()
     line = {
         "metric": "NVFP4 MoE-layer decode, %d tokens per call: us/token and achieved HBM GB/s" % Tb,
-        "value": us / Tb, "unit": "us/token", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": us * 1e-3,
+        "value": r["us_per_layer_call"] / Tb, "unit": "us/token", "n_gpus": 1, "steps": reps * n_inst,
+        "warmup": 3, "ms_per_step": r["us_per_layer_call"] * 1e-3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16-act/nvfp4-weight, bf16 MMA, f32 accumulate",
+        "dtype": "bf16-act/nvfp4-weight, f16 MMA, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
         "config": {"workload": "qwen3.6-35b-a3b-shaped MoE layer decode, T=%d tokens per call, H=2048 E=256 "
                                "top-8 I=512 shared Is=512, NVFP4 E4M3 per-16 scales, %d stacked layers with "
-                               "independent weights (%.1f GB resident)"
-                               % (Tb, n_inst, n_inst * 0.4531), "tokens_per_step": Tb,
+                               "independent weights (%.1f GB resident)" % (Tb, n_inst, n_inst * 0.4531),
+                   "tokens_per_step": Tb,
                    "l2": "inputs larger than L2: every layer's weights are read once per decode step"},
-        "us_per_call": us, "achieved_gbs": gbs,
-        "decode_step": {"layers": n_inst, "us": us * n_inst,
-                        "note": "one graph replay = the layer calls of one decode step through the stacked "
-                                "layers, in sequence on one stream; each layer gets its own seeded input "
-                                "(the pages' layer has no norm, so a raw chain underflows within a few layers "
-                                "and would route every token to the same experts)"},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak if peak else None, "peak_kind": peak_kind, "traffic": None,
-                     "bytes_per_launch": bytes_call,
+        "decode_step": r,
+        "roofline": {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": r["frac_of_hbm_peak"], "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": r["bytes_per_layer_call"],
                      "kernel": "whole call (router, route, gate/up, down, combine): algorithmic bytes / call time"},
-        "gpu_launches": nv.launches_per_layer_call(Tb, layers[0].H) * K,
-        "clocks": clk.summary(),
+        "gpu_launches": nv.launches_per_layer_call(Tb, layers[0].H) * reps * n_inst,
         "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_gemv(args, nv, wl, device):
+def measure_gemv(nv, wl, device, reps=10):
     """Dense NVFP4 W4A16 GEMV like a GatedDeltaNet in_proj_qkv: 1 token, K=2048 -> N=8192,
-    FP16 block scales (the value) and E4M3 block scales (reported beside). 16 packed
-    weight instances (168 MB) rotate so that every call reads cold weights; one CUDA
-    graph replays a pass over them. Bytes per call: codes, scales, tensor scale, x, y."""
+    FP16 block scales and E4M3 block scales. 16 packed weight instances (168 MB) rotate
+    so that every call reads cold weights; one CUDA graph replays a pass over them. Bytes
+    per call: codes, scales, tensor scale, x, y."""
     N, K, T = 8192, 2048, 1
     n_inst = 16
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peaks()
     res = {}
-    clk_summary = None
     for kind, name in ((nv.SCALE_FP16, "fp16"), (nv.SCALE_E4M3, "e4m3")):
-        Ws = []
-        for i in range(n_inst):
-            w = wl.dense_weight_f32(1 + i, N, K, device=device)
-            Ws.append(nv.nvfp4_pack(w, kind))
-            del w
+        Ws = [nv.nvfp4_pack(wl.dense_weight_f32(1 + i, N, K, device=device), kind) for i in range(n_inst)]
         xs = [wl.activations(1 + i, T, K, device=device) for i in range(n_inst)]
         ys = [torch.empty(T, N, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
         sb = 2 if kind == nv.SCALE_FP16 else 1
         bytes_call = N * K // 2 + N * (K // 16) * sb + 4 + 2 * K * T + 2 * N * T
-        cap = torch.cuda.Stream()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            for i in range(n_inst):
-                nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=cap):
-                for i in range(n_inst):
-                    nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])
-        torch.cuda.synchronize()
-        W = max(3, args.warmup)
-        for _ in range(W):
+        cap = torch.cuda.Stream(device=device)
+        g = graph_of([(lambda i=i: nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])) for i in range(n_inst)], cap)
+        for _ in range(3):
             g.replay()
-        torch.cuda.synchronize()
-        passes = max(1, -(-max(1, args.steps) // n_inst))
-        K_calls = passes * n_inst
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        with ClockSampler(device.index or 0) as clk:
-            time.sleep(0.3)
-            torch.cuda.synchronize()
-            ev0.record(stream)
-            for _ in range(passes):
-                g.replay()
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            time.sleep(0.2)
-        us = 1e3 * ev0.elapsed_time(ev1) / K_calls
+        ms, clk = time_graph(g, reps, stream, device, clocks=(kind == nv.SCALE_FP16))
+        us = 1e3 * ms / (reps * n_inst)
         gbs = bytes_call / (us * 1e-6) / 1e9
         res[name] = {"us_per_call": us, "bytes_per_call": bytes_call, "achieved_gbs": gbs,
-                     "frac_of_hbm_peak": gbs / peak if peak else None, "calls": K_calls}
-        if kind == nv.SCALE_FP16:
-            clk_summary = clk.summary()
+                     "frac_of_hbm_peak": gbs / peak if peak else None, "calls": reps * n_inst}
+        if clk:
+            res["clocks"] = clk
         del Ws, xs, ys, g
+    res["peak_kind"] = peak_kind
+    return res
+
+
+def run_gemv(args, nv, wl, device):
+    reps = max(1, -(-max(1, args.steps) // 16))
+    res = measure_gemv(nv, wl, device, reps)
     f = res["fp16"]
+    peak, peak_kind = measured_peaks()
     line = {
         "metric": "NVFP4 dense W4A16 GEMV, 1 token, K=2048 -> N=8192: us per call and achieved HBM GB/s",
-        "value": f["us_per_call"], "unit": "us/call", "n_gpus": 1, "steps": f["calls"], "warmup": max(3, args.warmup),
+        "value": f["us_per_call"], "unit": "us/call", "n_gpus": 1, "steps": f["calls"], "warmup": 3,
         "ms_per_step": f["us_per_call"] * 1e-3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16-act/nvfp4-weight, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
@@ -471,7 +521,7 @@ def run_gemv(args, nv, wl, device):
                      "bytes_per_launch": f["bytes_per_call"], "kernel": "gemv_kernel (one launch per call)"},
         "e4m3": res["e4m3"],
         "gpu_launches": f["calls"],
-        "clocks": clk_summary,
+        "clocks": res.get("clocks"),
         "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
@@ -508,9 +558,12 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
+    extras = rank == 0 and not args.no_extras
 
+    # layer instances: seeds 0..31 for the single-token steps; 40 stacked layers (seeds
+    # 0..39) for the decode-step figures of the default run
     n_inst = max(1, min(args.seeds, N_SEEDS))
-    layers, xs = build_layers(nv, wl, device, n_inst)
+    layers, xs = build_layers(nv, wl, device, CHAIN_LAYERS if extras and n_inst == N_SEEDS else n_inst)
     T = 1
     ws = nv.Workspace(nv.moe_layer_workspace_size(layers[0], T), device=device)
     descs = [l.desc() for l in layers]
@@ -528,47 +581,28 @@ def main():
         j = i % n_inst
         nv.moe_layer_forward(layers[j], xs[j], ws=ws, y=ys[j], desc=descs[j])
 
-    for i in range(max(3, args.warmup)):
+    W = max(3, args.warmup)
+    for i in range(W):
         step(i)
     torch.cuda.synchronize()
 
-    # One pass over every layer instance, captured once as a CUDA graph: the
-    # timed region replays it, so the host's per-call cost (Python, ctypes) does
-    # not leave the GPU idle between steps; consecutive kernels inside the graph
-    # keep their programmatic (PDL) dependency.
+    # Exactly K steps, captured once as one CUDA graph: the timed region is one replay,
+    # so the host's per-call cost (Python, ctypes) does not leave the GPU idle between
+    # steps; consecutive kernels inside the graph keep their programmatic (PDL)
+    # dependency. Steps rotate over the instances (14.5 GB >> L2).
+    K = max(1, args.steps)
     cap = torch.cuda.Stream(device=device)
     cap.wait_stream(stream)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        for i in range(n_inst):
-            step(i)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(graph, stream=cap):
-            for i in range(n_inst):
-                step(i)
-    torch.cuda.synchronize()
-    for _ in range(max(3, args.warmup // n_inst + 1)):
-        graph.replay()
+    graph = graph_of([(lambda i=i: step(i)) for i in range(K)], cap)
+    graph.replay()       # untimed: warms the graph itself
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-
-    reps = max(1, (args.steps + n_inst - 1) // n_inst)
-    K = reps * n_inst
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        time.sleep(0.3)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        time.sleep(0.2)
-    ms, us_per_token = replicas_timing(ev0.elapsed_time(ev1), K, world, device)
-    avg_bytes = sum(bytes_per_step) / n_inst
-    achieved_gbs = avg_bytes / (1e3 * ms / K * 1e-6) / 1e9
+    ms_local, clocks = time_graph(graph, 1, stream, device, clocks=True)
+    ms, us_per_token = replicas_timing(ms_local, K, world, device)
+    avg_bytes = sum(bytes_per_step[i % n_inst] for i in range(K)) / K
+    achieved_gbs = avg_bytes / (us_per_token * world * 1e-6) / 1e9
+    del graph
 
     # the same steps launched one by one from Python (host-bound; reported beside)
     Ks = min(K, 1000)
@@ -582,7 +616,7 @@ def main():
     stream_us = 1e3 * es0.elapsed_time(es1) / Ks
 
     # end to end through the public API with host buffers: pinned x in, y out, every step
-    xh = [x.cpu().pin_memory() for x in xs]
+    xh = [x.cpu().pin_memory() for x in xs[:n_inst]]
     yh = torch.empty(T, layers[0].H, dtype=torch.bfloat16).pin_memory()
     xd = torch.empty(T, layers[0].H, dtype=torch.bfloat16, device=device)
     for i in range(5):
@@ -603,68 +637,23 @@ def main():
     torch.cuda.synchronize()
     e2e_us = 1e3 * e0.elapsed_time(e1) / Ke
 
-    # batched decode: 8 and 64 tokens per call through the same rotating layers (the
-    # multi-token kernels), graph-replayed like the single-token steps
-    batched = []
-    for Tb in (8, 64):
-        xb = [wl.activations(100 + i, Tb, layers[0].H, device=device) for i in range(n_inst)]
-        wsb = nv.Workspace(nv.moe_layer_workspace_size(layers[0], Tb), device=device)
-        yb = [torch.empty(Tb, layers[0].H, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
-        idsb = []
-        for i in range(n_inst):
-            _, ids_i, _ = nv.moe_layer_forward(layers[i], xb[i], ws=wsb, want_route=True, desc=descs[i])
-            idsb.append(ids_i.cpu().numpy().ravel())
-        bytes_b = sum(step_bytes(layers[i], idsb[i], T=Tb) for i in range(n_inst)) / n_inst
-        gb = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            for i in range(n_inst):
-                nv.moe_layer_forward(layers[i], xb[i], ws=wsb, y=yb[i], desc=descs[i])
-            torch.cuda.synchronize()
-            with torch.cuda.graph(gb, stream=cap):
-                for i in range(n_inst):
-                    nv.moe_layer_forward(layers[i], xb[i], ws=wsb, y=yb[i], desc=descs[i])
-        torch.cuda.synchronize()
-        for _ in range(3):
-            gb.replay()
-        torch.cuda.synchronize()
-        rb = max(1, 200 // n_inst)
-        b0 = torch.cuda.Event(enable_timing=True)
-        b1 = torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for _ in range(rb):
-            gb.replay()
-        b1.record(stream)
-        torch.cuda.synchronize()
-        us_call = 1e3 * b0.elapsed_time(b1) / (rb * n_inst)
-        gbs = bytes_b / (us_call * 1e-6) / 1e9
-        batched.append({"tokens": Tb, "us_per_call": us_call, "us_per_token": us_call / Tb,
-                        "bytes_per_call": bytes_b, "achieved_gbs": gbs})
-        del wsb
-
+    if world > 1:
+        dist.barrier()
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
+        dist.destroy_process_group()
         return 0
 
     peak, peak_kind = measured_peaks()
-    for b in batched:
-        b["frac_of_hbm_peak"] = b["achieved_gbs"] / peak if peak else None
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        us, n, tot = cpu_oracle_sample(args.cpu_seconds)
-        cpu = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d single-token layer calls of the same workload (seeds 0..%d), %.1f s" %
-                         (n, min(n, N_SEEDS) - 1, tot)}
-    launches_per_step = nv.launches_per_layer_call(T, layers[0].H)
     line = {
         "metric": METRIC, "value": us_per_token, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": False,
+        "warmup": W, "ms_per_step": ms / K, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16-act/nvfp4-weight, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
         "config": {"workload": WORKLOAD, "tokens_per_step": 1,
                    "l2": "inputs larger than L2: %d rotating layer instances (%.1f GB)" % (
-                       n_inst, sum(l.gu_packed.numel() + l.dn_packed.numel() for l in layers) * 1.125 / 1e9),
+                       n_inst, sum(l.gu_packed.numel() + l.dn_packed.numel() for l in layers[:n_inst]) * 1.125 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": 1e6 / us_per_token,
         "achieved_gbs": achieved_gbs,
         "pct_of_8tbs": 100.0 * achieved_gbs / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
@@ -673,13 +662,25 @@ def main():
                      "kernel": "moe_decode_t1_kernel (the whole step is this one launch)"},
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": 2 * layers[0].H * T,
                 "d2h_bytes_per_step": 2 * layers[0].H * T},
-        "gpu_launches": launches_per_step * K,
-        "timing": {"mode": "CUDA graph replay of %d-step passes" % n_inst,
+        "gpu_launches": nv.launches_per_layer_call(T, layers[0].H) * K,
+        "timing": {"mode": "one CUDA graph of exactly %d steps, replayed once" % K,
                    "stream_launch_us_per_token": stream_us},
-        "batched_decode": batched,
-        "clocks": clk.summary(),
-        "cpu_baseline": cpu,
+        "clocks": clocks,
     }
+    if extras:
+        # the other measured configurations, each with its own CUDA-event timing
+        line["batched_decode"] = [measure_batched(nv, wl, device, layers[:n_inst], descs[:n_inst], Tb, True, stream)
+                                  for Tb in (8, 64)]
+        if len(layers) == CHAIN_LAYERS:
+            line["decode_step_40_layers"] = [measure_batched(nv, wl, device, layers, descs, Tb, False, stream)
+                                             for Tb in (1, 8, 64)]
+        del layers, xs, ys, ws, descs
+        torch.cuda.empty_cache()
+        line["gemv"] = measure_gemv(nv, wl, device)
+        line["prefill"] = measure_prefill(nv, wl, device, steps=20, warmup=3)
+    line["cpu_baseline"] = None
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_block(args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

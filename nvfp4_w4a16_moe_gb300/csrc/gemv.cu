@@ -210,9 +210,14 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
             int issued = 0;
             for (int v = 0; v < nv; ++v) {
                 const int slot = v % p.slots;
-                if (v >= p.slots &&
-                    !mbar_wait_bounded(&empty[slot], (uint32_t)((v / p.slots) - 1) & 1u, p.wait_limit))
-                    break;   // the consumers time out on the missing chunks and record it
+                if (v >= p.slots) {
+                    if (!mbar_wait_bounded(&empty[slot], (uint32_t)((v / p.slots) - 1) & 1u, p.wait_limit))
+                        break;   // the consumers time out on the missing chunks and record it
+                    // a consumer that timed out releases its slot without waiting for the copy:
+                    // never refill a slot whose previous copy is still in flight
+                    if (!mbar_wait_bounded(&full[slot], (uint32_t)((v / p.slots) - 1) & 1u, kDefaultWaitLimit))
+                        break;
+                }
                 const int r0 = (g0 + v % nc) * kCRows;
                 const int nr = min(kCRows, N - r0);
                 const uint32_t pb = (uint32_t)nr * rowB;                 // a multiple of 16
@@ -223,9 +228,10 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                 if (scb) bulk_g2s(dst + off_sc, p.scales + (size_t)r0 * srowB, scb, &full[slot]);
                 issued = v + 1;
             }
-            // drain: the last fill of every slot has landed before the CTA may exit
+            // drain: the last fill of every slot has landed before the CTA may exit (with the
+            // library's fixed limit, not the caller's: copies in flight always land)
             for (int v = max(0, issued - p.slots); v < issued; ++v)
-                mbar_wait_bounded(&full[v % p.slots], (uint32_t)(v / p.slots) & 1u, p.wait_limit);
+                mbar_wait_bounded(&full[v % p.slots], (uint32_t)(v / p.slots) & 1u, kDefaultWaitLimit);
         }
         return;
     }

@@ -14,14 +14,16 @@ range and every later layer computes zeros. Two chains are therefore run:
   later ones for finiteness and the absolute part of the bar.
 
 Parity is per layer, teacher-forced: the oracle gets the GPU's bf16 input of that
-layer. Besides the usual bar (max|gpu - oracle| <= 1e-2 max|oracle| + 1e-3) each
-checked layer meets the scale-free bound max|gpu - oracle| <= 2e-2 max|oracle|.
+layer. Every layer and every token is checked (the oracle's experts run in
+spawned worker processes, all layers in flight at once). Besides the usual bar
+(max|gpu - oracle| <= 1e-2 max|oracle| + 1e-3) each checked layer meets the
+scale-free bound max|gpu - oracle| <= 2e-2 max|oracle|.
 """
 import pytest
 import torch
 
 import workload as wl
-from harness import check_layer_parity, gpu_layer, oracle_layer
+from harness import ParityCheck, check_layer_parity, gpu_layer, oracle_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -58,35 +60,35 @@ def _run_chain(nv, layers, x0, renorm):
     return xs, outs
 
 
-def _check(l, x, y, ids, w, rows=None):
-    L = wl.LayerInputs(QW, seed=SEED, layer=l)
-    if rows is not None:
-        idx = torch.tensor(rows, dtype=torch.long)
-        x, y, ids, w = x[idx], y.cpu()[idx], ids.cpu()[idx], w.cpu()[idx]
-    check_layer_parity(L, x, y, ids, w, rel_only=2e-2)
+def _check(l, x, y, ids, w):
+    check_layer_parity(wl.LayerInputs(QW, seed=SEED, layer=l), x, y, ids, w, rel_only=2e-2)
+
+
+def _check_all_layers(xs, outs):
+    checks = [ParityCheck(wl.LayerInputs(QW, seed=SEED, layer=l), xs[l], *outs[l], rel_only=2e-2)
+              for l in range(N_LAYERS)]
+    for c in checks:
+        c.check()
 
 
 def test_chain_40_layers_one_token(nv, chain):
     x0 = wl.activations(SEED, 1, QW.H)
     xs, outs = _run_chain(nv, chain, x0, renorm=True)
-    for l in range(N_LAYERS):
-        _check(l, xs[l], *outs[l])
+    _check_all_layers(xs, outs)
 
 
 def test_chain_40_layers_8_tokens(nv, chain):
     x0 = wl.activations(SEED + 1, 8, QW.H)
     xs, outs = _run_chain(nv, chain, x0, renorm=True)
     assert all(torch.isfinite(o[0].float()).all() for o in outs)
-    for l in (0, 13, 26, 39):
-        _check(l, xs[l], *outs[l])
+    _check_all_layers(xs, outs)
 
 
 def test_chain_40_layers_64_tokens(nv, chain):
     x0 = wl.activations(SEED + 2, 64, QW.H)
     xs, outs = _run_chain(nv, chain, x0, renorm=True)
     assert all(torch.isfinite(o[0].float()).all() for o in outs)
-    for l in (0, 39):
-        _check(l, xs[l], *outs[l], rows=[0, 9, 31, 32, 50, 63])
+    _check_all_layers(xs, outs)
 
 
 def test_chain_40_layers_raw(nv, chain):

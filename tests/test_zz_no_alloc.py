@@ -2,7 +2,8 @@
 instead of a caller workspace, for callers that cannot allocate device memory
 where they run the layer. Checked through the C ABI against moe_layer_forward
 on the same inputs, two calls in a row, for the one-launch single-token path
-and the multi-token path. This file is collected last on purpose."""
+and the multi-token path. Both entry points run the same deterministic kernels,
+so the outputs must agree bit for bit. This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -28,7 +29,8 @@ def _noalloc(nv, layer, x):
     return y, ids, w
 
 
-@pytest.mark.parametrize("shape,T", [(wl.TINY, 1), (wl.TINY, 5), (wl.QWEN36_35B_A3B, 1), (wl.QWEN36_35B_A3B, 64)])
+@pytest.mark.parametrize("shape,T", [(wl.TINY, 1), (wl.SMALL256, 1), (wl.TINY, 5), (wl.QWEN36_35B_A3B, 1),
+                                     (wl.QWEN36_35B_A3B, 64)])
 def test_noalloc_matches_workspace_entry_point(nv, shape, T):
     L = wl.LayerInputs(shape, seed=7)
     layer = gpu_layer(L)
@@ -40,8 +42,24 @@ def test_noalloc_matches_workspace_entry_point(nv, shape, T):
         ok, err, bound = tol_ok(y.float().cpu().numpy().astype(np.float64),
                                 y_ref.float().cpu().numpy().astype(np.float64))
         assert ok, (err, bound)
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
         assert torch.equal(ids, ids_ref)
-        assert torch.allclose(w, w_ref, atol=1e-6)
+        assert torch.equal(w, w_ref)
+
+
+def test_noalloc_large_then_small_then_large(nv):
+    """A smaller call after a larger one, then a larger one with other inputs: what the
+    previous call left in the shared scratch must not leak into the next result."""
+    shape = wl.QWEN36_35B_A3B
+    L = wl.LayerInputs(shape, seed=8)
+    layer = gpu_layer(L)
+    for T, seed in ((64, 8), (1, 9), (64, 10), (8, 11), (1, 12)):
+        x = wl.activations(seed, T, shape.H).cuda()
+        y_ref, ids_ref, w_ref = nv.moe_layer_forward(layer, x, want_route=True)
+        y, ids, w = _noalloc(nv, layer, x)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), T
+        assert torch.equal(ids, ids_ref) and torch.equal(w, w_ref), T
 
 
 def test_noalloc_rejects_oversized_scratch(nv):
