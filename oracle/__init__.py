@@ -71,6 +71,10 @@ def lib():
         L.orc_route.argtypes = [P, i32, i32, i32, P, P, P]
         L.orc_swiglu.restype = None
         L.orc_swiglu.argtypes = [P, P, f32, P, P, f32, P, P, f32, i32, i32, i32, P, i32, P]
+        L.orc_bf16_from_double.restype = ctypes.c_uint16
+        L.orc_bf16_from_double.argtypes = [ctypes.c_double]
+        L.orc_rmsnorm.restype = None
+        L.orc_rmsnorm.argtypes = [P, i32, i32, P, ctypes.c_double, P, P]
         L.orc_moe_layer.restype = i32
         L.orc_moe_layer.argtypes = ([i32] * 6 + [P, i32, P, P] + [P, P, P] * 3 +
                                     [P, P, f32] * 3 + [P, P, P, P, P])
@@ -371,3 +375,38 @@ def moe_layer_batched(x, router_w, sh_gate_vec, experts: dict, shared, k: int, f
         srows = swiglu_rows(*shared, xr)
     y = combine(rows, w, srows, sig if shared is not None else None)
     return LayerResult(y, ids, w, sig)
+
+
+# ------------------------------------------------- the layer in the residual stream
+
+def bf16_from_double(v: float) -> int:
+    """bits of the bf16 nearest to v (ties to even), rounded directly from fp64."""
+    return int(lib().orc_bf16_from_double(float(v)))
+
+
+def rmsnorm(h, w, eps: float):
+    """(bf16 bits [T, H], fp64 values before rounding) of (1 + w) * h / sqrt(mean(h^2) + eps)
+    (lynn-engine tutorials index, row 01)."""
+    hb = _np(h, np.uint16)
+    wb = _np(w, np.uint16)
+    T, H = hb.shape
+    out = np.zeros((T, H), np.uint16)
+    f = np.zeros((T, H), np.float64)
+    lib().orc_rmsnorm(_ptr(hb), T, H, _ptr(wb), float(eps), _ptr(out), _ptr(f))
+    return out, f
+
+
+def moe_layer_residual(h, norm_w, eps, router_w, sh_gate_vec, experts: dict, shared, k: int,
+                       force_ids=None, batched: bool = False) -> LayerResult:
+    """The MoE layer inside the residual stream: x = bf16(RMSNorm_(1+w)(h)), then
+    y = h + moe_layer(x) in fp64 (README "decode launch-overhead campaign": fused RMSNorm;
+    Lynn write-up, "Fused Kernels"). ``batched`` evaluates the layer with
+    moe_layer_batched instead of the per-token C code."""
+    xb, _ = rmsnorm(h, norm_w, eps)
+    if batched:
+        res = moe_layer_batched(xb, router_w, sh_gate_vec, experts, shared, k, force_ids=force_ids)
+    else:
+        res = moe_layer(xb, router_w, sh_gate_vec, experts, shared, k, force_ids=force_ids)
+    res.y = res.y + bf16_rows(h)
+    res.x = xb
+    return res

@@ -421,3 +421,51 @@ int orc_moe_layer(int H, int E, int k, int I, int Is, int kind, const uint16_t* 
     free(logits); free(probs); free(ids); free(w); free(xv); free(ht); free(o);
     return rc;
 }
+
+/* ------------------------------------------------------------ pre-MoE norm */
+
+/* Round a double to the nearest bf16 (ties to even); returns the bf16 bits. Values
+ * beyond bf16's range become +-inf, NaN stays NaN. Direct rounding from fp64 (no
+ * intermediate fp32 step). */
+uint16_t orc_bf16_from_double(double v) {
+    if (isnan(v)) return 0x7FC0;
+    int sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return (uint16_t)sign;
+    /* bf16: 8 significant bits, exponent range of fp32 (normal min 2^-126, subnormal step 2^-133) */
+    int ex;
+    frexp(a, &ex);                       /* a = f * 2^ex, f in [0.5, 1) */
+    int E = ex - 1;                      /* a in [2^E, 2^(E+1)) */
+    if (E < -126) E = -126;              /* subnormal: fixed quantum 2^-133 */
+    double q = ldexp(a, 7 - E);          /* units of 2^(E-7) */
+    double r = nearbyint(q);             /* ties to even (default rounding mode) */
+    double back = ldexp(r, E - 7);
+    if (back >= 0x1.FF8p127) return (uint16_t)(sign | 0x7F80);   /* rounds past the largest bf16 */
+    /* encode back (exact in fp32) */
+    float f = (float)back;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* RMSNorm in the (1 + weight) form (lynn-engine tutorials index, row 01: RMSNorm =
+ * (1.0 + weight) x x_norm; the Qwen 3.6 config block: rms_norm (1.0 + weight) x x_norm):
+ *   x_norm[t,i] = h[t,i] / sqrt(mean_i h[t,i]^2 + eps),  out[t,i] = bf16((1 + w[i]) * x_norm[t,i])
+ * All arithmetic in fp64; one rounding to bf16 (the activation type the layer consumes).
+ * out_f64 (nullable) receives the value before that rounding. */
+void orc_rmsnorm(const uint16_t* h, int T, int H, const uint16_t* w, double eps, uint16_t* out,
+                 double* out_f64) {
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int i = 0; i < H; ++i) {
+            double v = bf16_to_double(h[(size_t)t * H + i]);
+            ss += v * v;
+        }
+        double r = 1.0 / sqrt(ss / (double)H + eps);
+        for (int i = 0; i < H; ++i) {
+            double v = bf16_to_double(h[(size_t)t * H + i]) * r * (1.0 + bf16_to_double(w[i]));
+            if (out_f64) out_f64[(size_t)t * H + i] = v;
+            out[(size_t)t * H + i] = orc_bf16_from_double(v);
+        }
+    }
+}
