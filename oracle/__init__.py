@@ -23,6 +23,12 @@ LIB = os.path.join(HERE, "_liboracle.so")
 
 SCALE_E4M3 = 0
 SCALE_FP16 = 1
+SCALE_FP32 = 2     # fp32 block scale per 16 elements, tensor scale 1
+SCALE_UE8M0 = 3    # power-of-two E8M0 scale per 32 elements, tensor scale 1
+
+# block length and numpy dtype of one block scale, per kind
+SCALE_BLOCK = {SCALE_E4M3: 16, SCALE_FP16: 16, SCALE_FP32: 16, SCALE_UE8M0: 32}
+SCALE_DTYPE = {SCALE_E4M3: np.uint8, SCALE_FP16: np.uint16, SCALE_FP32: np.float32, SCALE_UE8M0: np.uint8}
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
           "-Wall", "-Wextra", "-Wno-unused-parameter"]
@@ -59,6 +65,8 @@ def lib():
         L.orc_fp16_decode.argtypes = [i32]
         L.orc_fp16_encode.restype = i32
         L.orc_fp16_encode.argtypes = [f32]
+        L.orc_e8m0_decode.restype = ctypes.c_double
+        L.orc_e8m0_decode.argtypes = [i32]
         L.orc_pack.restype = i32
         L.orc_pack.argtypes = [P, i32, i32, i32, P, P, P]
         L.orc_dequant.restype = None
@@ -123,9 +131,14 @@ def fp16_encode(v: float) -> int:
     return lib().orc_fp16_encode(float(v))
 
 
+def e8m0_decode(b: int) -> float:
+    return lib().orc_e8m0_decode(int(b))
+
+
 @dataclass
 class Packed:
-    """One NVFP4 matrix: packed [N, K/2] u8, scales [N, K/16] (u8 E4M3 or u16 FP16), fp32 tensor scale."""
+    """One NVFP4 matrix: packed [N, K/2] u8, scales [N, K/B] (u8 E4M3, u16 FP16, f32 FP32 with B = 16;
+    u8 E8M0 with B = 32), fp32 tensor scale."""
     packed: np.ndarray
     scales: np.ndarray
     tensor_scale: float
@@ -138,7 +151,7 @@ def pack(w, kind: int = SCALE_E4M3) -> Packed:
     w = _np(w, np.float32)
     N, K = w.shape
     packed = np.zeros((N, K // 2), np.uint8)
-    scales = np.zeros((N, K // 16), np.uint8 if kind == SCALE_E4M3 else np.uint16)
+    scales = np.zeros((N, K // SCALE_BLOCK[kind]), SCALE_DTYPE[kind])
     ts = np.zeros(1, np.float32)
     rc = lib().orc_pack(_ptr(w), N, K, kind, _ptr(packed), _ptr(scales), _ptr(ts))
     if rc != 0:
@@ -279,8 +292,12 @@ def _decode_tables(kind: int):
         e2m1 = np.array([e2m1_decode(c) for c in range(16)], np.float64)
         if kind == SCALE_E4M3:
             sc = np.array([e4m3_decode(b) for b in range(256)], np.float64)
-        else:
+        elif kind == SCALE_UE8M0:
+            sc = np.array([e8m0_decode(b) for b in range(256)], np.float64)
+        elif kind == SCALE_FP16:
             sc = np.array([fp16_decode(b) for b in range(65536)], np.float64)
+        else:
+            sc = None   # fp32 scales are their own values
         t = (e2m1, sc)
         _TABLES[kind] = t
     return t
@@ -292,7 +309,8 @@ def dequant_table(p: Packed) -> np.ndarray:
     codes = np.empty((p.N, p.K), np.uint8)
     codes[:, 0::2] = p.packed & 15
     codes[:, 1::2] = p.packed >> 4
-    s = np.repeat(sc[p.scales.astype(np.int64)], 16, axis=1)
+    vals = p.scales.astype(np.float64) if sc is None else sc[p.scales.astype(np.int64)]
+    s = np.repeat(vals, SCALE_BLOCK[p.kind], axis=1)
     return e2m1[codes] * s * float(p.tensor_scale)
 
 
@@ -406,7 +424,8 @@ def moe_layer_residual(h, norm_w, eps, router_w, sh_gate_vec, experts: dict, sha
     if batched:
         res = moe_layer_batched(xb, router_w, sh_gate_vec, experts, shared, k, force_ids=force_ids)
     else:
-        res = moe_layer(xb, router_w, sh_gate_vec, experts, shared, k, force_ids=force_ids)
+        kind = next(iter(experts.values()))[0].kind if experts else SCALE_E4M3
+        res = moe_layer(xb, router_w, sh_gate_vec, experts, shared, k, kind=kind, force_ids=force_ids)
     res.y = res.y + bf16_rows(h)
     res.x = xb
     return res

@@ -44,6 +44,8 @@
 
 #define ORC_SCALE_E4M3 0
 #define ORC_SCALE_FP16 1
+#define ORC_SCALE_FP32 2    /* fp32 block scale per 16 elements, tensor scale 1 (README P52) */
+#define ORC_SCALE_UE8M0 3   /* power-of-two E8M0 scale per 32 elements, tensor scale 1 (README P17/P18) */
 
 #define ORC_OK 0
 #define ORC_ERR_ARG 1
@@ -151,19 +153,38 @@ static double bf16_to_double(uint16_t b) {
     return (double)f;
 }
 
+/* E8M0 (OCP MX shared scale): 2^(byte - 127); 0xFF is NaN. */
+double orc_e8m0_decode(int byte) {
+    if ((byte & 0xFF) == 0xFF) return NAN;
+    return ldexp(1.0, (byte & 0xFF) - 127);
+}
+
+/* Elements per scale block of a scale kind. */
+static int block_elems(int kind) { return kind == ORC_SCALE_UE8M0 ? 32 : 16; }
+
 static double scale_value(const void* scales, int kind, size_t idx) {
     if (kind == ORC_SCALE_E4M3) return orc_e4m3_decode(((const uint8_t*)scales)[idx]);
+    if (kind == ORC_SCALE_FP32) return (double)((const float*)scales)[idx];
+    if (kind == ORC_SCALE_UE8M0) return orc_e8m0_decode(((const uint8_t*)scales)[idx]);
     return orc_fp16_decode(((const uint16_t*)scales)[idx]);
 }
 
 /* -------------------------------------------------------------------- pack */
 
-/* Quantise fp32 W[N,K] (row-major) to NVFP4: packed [N,K/2], scales [N,K/16]
- * (one byte E4M3 or one uint16 FP16 each), one fp32 tensor scale. */
+/* Quantise fp32 W[N,K] (row-major) to NVFP4: packed [N,K/2], scales [N,K/B] (B = 16, or
+ * 32 for UE8M0), one fp32 tensor scale. Per scale kind:
+ *   E4M3   s_t = amax(W)/(6*448) (1 if amax = 0); block code = E4M3_rne_satfinite((amax_b/6)/s_t)
+ *   FP16   s_t = 1; block code = FP16_rne_satfinite(amax_b/6)
+ *   FP32   s_t = 1; block scale = amax_b/6 (one fp32 division)
+ *   UE8M0  s_t = 1; block exponent = floor(log2(amax_b)) - 2 (the OCP MX rule: the largest
+ *          power of two of E2M1 is 2^2), clamped to the E8M0 range [-127, 127]; 0 for amax_b = 0
+ * and every element becomes the E2M1 code nearest to w / (decoded block scale * s_t). */
 int orc_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scales,
              float* tensor_scale) {
-    if (N < 0 || K < 0 || K % 16 != 0) return ORC_ERR_ARG;
-    if (kind != ORC_SCALE_E4M3 && kind != ORC_SCALE_FP16) return ORC_ERR_ARG;
+    if (kind != ORC_SCALE_E4M3 && kind != ORC_SCALE_FP16 && kind != ORC_SCALE_FP32 && kind != ORC_SCALE_UE8M0)
+        return ORC_ERR_ARG;
+    const int B = block_elems(kind);
+    if (N < 0 || K < 0 || K % B != 0) return ORC_ERR_ARG;
     size_t total = (size_t)N * K;
     float amax_t = 0.0f;
     for (size_t i = 0; i < total; ++i) {
@@ -174,12 +195,12 @@ int orc_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scal
     float s_t = 1.0f;
     if (kind == ORC_SCALE_E4M3 && amax_t > 0.0f) s_t = amax_t / 2688.0f;
     *tensor_scale = s_t;
-    int nb = K / 16;
+    int nb = K / B;
     for (int n = 0; n < N; ++n) {
         for (int b = 0; b < nb; ++b) {
-            const float* blk = w + (size_t)n * K + (size_t)b * 16;
+            const float* blk = w + (size_t)n * K + (size_t)b * B;
             float amax_b = 0.0f;
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < B; ++i) {
                 float a = fabsf(blk[i]);
                 if (a > amax_b) amax_b = a;
             }
@@ -190,13 +211,27 @@ int orc_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scal
                 int e = orc_e4m3_encode(r / s_t);
                 ((uint8_t*)scales)[sidx] = (uint8_t)e;
                 dec = (float)orc_e4m3_decode(e) * s_t;
-            } else {
+            } else if (kind == ORC_SCALE_FP16) {
                 int e = orc_fp16_encode(r);
                 ((uint16_t*)scales)[sidx] = (uint16_t)e;
                 dec = (float)orc_fp16_decode(e) * s_t;
+            } else if (kind == ORC_SCALE_FP32) {
+                ((float*)scales)[sidx] = r;
+                dec = r;
+            } else {
+                int ex = 0;
+                if (amax_b > 0.0f) {
+                    int fe;
+                    frexpf(amax_b, &fe);         /* amax_b = f * 2^fe, f in [0.5, 1) */
+                    ex = (fe - 1) - 2;           /* floor(log2(amax_b)) - 2 */
+                    if (ex < -127) ex = -127;
+                    if (ex > 127) ex = 127;
+                }
+                ((uint8_t*)scales)[sidx] = (uint8_t)(ex + 127);
+                dec = ldexpf(1.0f, ex);
             }
-            uint8_t* out = packed + (size_t)n * (K / 2) + (size_t)b * 8;
-            for (int j = 0; j < 8; ++j) {
+            uint8_t* out = packed + (size_t)n * (K / 2) + (size_t)b * (B / 2);
+            for (int j = 0; j < B / 2; ++j) {
                 int lo = 0, hi = 0;
                 if (dec > 0.0f) {
                     lo = orc_e2m1_encode(blk[2 * j] / dec);
@@ -214,13 +249,14 @@ int orc_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scal
 /* W[n,k] = E2M1(code) * scale(n, k/16) * tensor_scale, in fp64 (exact). */
 void orc_dequant(const uint8_t* packed, const void* scales, float tensor_scale, int kind,
                  int N, int K, double* out) {
-    int nb = K / 16;
+    const int B = block_elems(kind);
+    int nb = K / B;
     for (int n = 0; n < N; ++n)
         for (int k = 0; k < K; ++k) {
             uint8_t byte = packed[(size_t)n * (K / 2) + k / 2];
             int code = (k & 1) ? (byte >> 4) : (byte & 15);
             out[(size_t)n * K + k] = orc_e2m1_decode(code) *
-                                     scale_value(scales, kind, (size_t)n * nb + k / 16) *
+                                     scale_value(scales, kind, (size_t)n * nb + k / B) *
                                      (double)tensor_scale;
         }
 }
@@ -228,12 +264,13 @@ void orc_dequant(const uint8_t* packed, const void* scales, float tensor_scale, 
 /* Dot product of dequantised row n with an fp64 vector v[K]. */
 static double row_dot(const uint8_t* packed, const void* scales, float ts, int kind, int n,
                       int K, const double* v) {
-    int nb = K / 16;
+    const int B = block_elems(kind);
+    int nb = K / B;
     double acc = 0.0;
     for (int k = 0; k < K; ++k) {
         uint8_t byte = packed[(size_t)n * (K / 2) + k / 2];
         int code = (k & 1) ? (byte >> 4) : (byte & 15);
-        double wv = orc_e2m1_decode(code) * scale_value(scales, kind, (size_t)n * nb + k / 16) *
+        double wv = orc_e2m1_decode(code) * scale_value(scales, kind, (size_t)n * nb + k / B) *
                     (double)ts;
         acc += wv * v[k];
     }

@@ -22,7 +22,7 @@ def _rand_packed(kind, N, K, key, scale_exp=0):
     return oracle.pack(w, kind)
 
 
-@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3])
 @pytest.mark.parametrize("scale_exp", [-30, 0, 20])
 def test_table_dequant_is_bit_exact(orc, kind, scale_exp):
     p = _rand_packed(kind, 33, 96, 7 + kind, scale_exp)

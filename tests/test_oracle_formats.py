@@ -208,3 +208,84 @@ def test_p1_packed_footprint(orc):
     packed_mib = bytes_per_elem * N * K / 2 ** 20
     assert packed_mib == pytest.approx(g["packed_mib"], abs=0.005)
     assert 2 * N * K / 2 ** 20 == pytest.approx(g["bf16_mib"], abs=0.005)
+
+
+# ------------------------------------------------------------------ other scale contracts
+# README P52 (Lynn-native fp32 scale per 16 elements) and P17/P18 (the e8m0 scale per 32
+# elements of the vendor MX layout, neutral byte 127).
+
+def test_e8m0_decode_all_bytes(orc):
+    for b in range(255):
+        assert orc.e8m0_decode(b) == 2.0 ** (b - 127)
+    assert np.isnan(orc.e8m0_decode(255))
+    assert orc.e8m0_decode(127) == 1.0
+
+
+def test_fp32_scale_on_grid_round_trip(orc):
+    """codes x an fp32 block scale whose block holds a +-6: the packer recovers both exactly."""
+    rng = np.random.default_rng(11)
+    N, K = 6, 64
+    codes = rng.integers(0, 16, size=(N, K))
+    codes[:, ::16] = 7                                   # a 6 in every block
+    s = (rng.integers(1, 2 ** 10, size=(N, K // 16)) * 2.0 ** rng.integers(-20, 5, size=(N, K // 16)))
+    s = s.astype(np.float32)
+    mags = np.array([orc.e2m1_decode(int(c)) for c in codes.ravel()]).reshape(N, K)
+    W = (mags * np.repeat(s.astype(np.float64), 16, axis=1)).astype(np.float32)
+    p = orc.pack(W, orc.SCALE_FP32)
+    assert p.tensor_scale == 1.0 and p.scales.dtype == np.float32
+    assert np.array_equal(p.scales, s)
+    got = np.empty((N, K), np.int64)
+    got[:, 0::2] = p.packed & 15
+    got[:, 1::2] = p.packed >> 4
+    zero = mags == 0
+    assert np.array_equal(got[~zero], codes[~zero])
+    assert np.array_equal(orc.dequant(p), W.astype(np.float64))
+
+
+def test_ue8m0_scale_on_grid_round_trip(orc):
+    """codes x 2^e per 32-element block whose largest magnitude is 4 or 6: the scale byte is
+    e + 127 (floor(log2 amax) - 2 = e) and every code comes back."""
+    rng = np.random.default_rng(12)
+    N, K = 5, 96
+    codes = rng.integers(0, 16, size=(N, K))
+    codes[:, ::32] = rng.choice([6, 7, 14, 15], size=(N, K // 32))   # largest magnitude 4 or 6
+    codes[:, 1::32] = 6
+    e = rng.integers(-30, 20, size=(N, K // 32))
+    mags = np.array([orc.e2m1_decode(int(c)) for c in codes.ravel()]).reshape(N, K)
+    W = (mags * np.repeat(2.0 ** e, 32, axis=1)).astype(np.float32)
+    p = orc.pack(W, orc.SCALE_UE8M0)
+    assert p.tensor_scale == 1.0 and p.scales.shape == (N, K // 32)
+    assert np.array_equal(p.scales.astype(np.int64), e + 127)
+    got = np.empty((N, K), np.int64)
+    got[:, 0::2] = p.packed & 15
+    got[:, 1::2] = p.packed >> 4
+    zero = mags == 0
+    assert np.array_equal(got[~zero], codes[~zero])
+    assert np.array_equal(orc.dequant(p), W.astype(np.float64))
+
+
+@pytest.mark.parametrize("kind", [2, 3])
+def test_new_kinds_codes_are_nearest(orc, kind):
+    """Random matrices: every code is the E2M1 point nearest to w / decoded block scale (ties
+    to the even code), and for UE8M0 the block's amax / scale lies in [4, 8)."""
+    B = 32 if kind == 3 else 16
+    w = wl.normal(wl.stream_key(13, kind), 20 * 128, 0.3).view(20, 128).numpy()
+    p = orc.pack(w, kind)
+    grid = np.array([orc.e2m1_decode(c) for c in range(8)])
+    sc = p.scales.astype(np.float64) if kind == 2 else 2.0 ** (p.scales.astype(np.float64) - 127)
+    full = np.repeat(sc, B, axis=1)
+    u = np.abs(w.astype(np.float64)) / full
+    codes = np.empty(w.shape, np.int64)
+    codes[:, 0::2] = p.packed & 15
+    codes[:, 1::2] = p.packed >> 4
+    for (n, k), uv in np.ndenumerate(u):
+        d = np.abs(grid - min(uv, 6.0))
+        best = np.flatnonzero(d == d.min())
+        m = codes[n, k] & 7
+        assert m in best, (n, k, uv, m)
+        if len(best) > 1:
+            assert m % 2 == 0
+    if kind == 3:
+        amax = np.abs(w).reshape(20, 128 // 32, 32).max(axis=2)
+        ratio = amax / sc
+        assert np.all((ratio >= 4) & (ratio < 8))
