@@ -83,7 +83,10 @@ def ncu_traffic():
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    src = open(os.path.join(ROOT, d["source"]), "rb").read()
+    sp = os.path.join(ROOT, d["source"])
+    if not os.path.exists(sp):
+        return None
+    src = open(sp, "rb").read()
     if hashlib.sha256(src).hexdigest()[:16] != d["source_sha256_prefix"]:
         return None
     return d["dram_bytes_read"] + d["dram_bytes_write"]
@@ -498,6 +501,32 @@ def measure_gemv(nv, wl, device, reps=10):
         if clk:
             res["clocks"] = clk
         del Ws, xs, ys, g
+    # the lm_head of the same model: vocab 248320 x hidden 2048 (318 / 287 MB per call, two
+    # instances rotating, each larger than L2)
+    N, n_inst = 248320, 2
+    for kind, name in ((nv.SCALE_FP16, "lm_head_fp16"), (nv.SCALE_E4M3, "lm_head_e4m3")):
+        Ws = []
+        for i in range(n_inst):
+            w = wl.dense_weight_f32(40 + i, N, K, device=device)
+            Ws.append(nv.nvfp4_pack(w, kind))
+            del w
+        xs = [wl.activations(40 + i, T, K, device=device) for i in range(n_inst)]
+        ys = [torch.empty(T, N, dtype=torch.bfloat16, device=device) for _ in range(n_inst)]
+        sb = 2 if kind == nv.SCALE_FP16 else 1
+        bytes_call = N * K // 2 + N * (K // 16) * sb + 4 + 2 * K * T + 2 * N * T
+        cap = torch.cuda.Stream(device=device)
+        g = graph_of([(lambda i=i: nv.nvfp4_gemv_w4a16(Ws[i], xs[i], y=ys[i])) for i in range(n_inst)], cap)
+        for _ in range(3):
+            g.replay()
+        r2 = max(4, reps)
+        ms, _ = time_graph(g, r2, stream, device)
+        us = 1e3 * ms / (r2 * n_inst)
+        gbs = bytes_call / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": us, "bytes_per_call": bytes_call, "achieved_gbs": gbs,
+                     "frac_of_hbm_peak": gbs / peak if peak else None, "calls": r2 * n_inst,
+                     "shape": "T=1, K=2048 -> N=248320"}
+        del Ws, xs, ys, g
+        torch.cuda.empty_cache()
     res["peak_kind"] = peak_kind
     return res
 

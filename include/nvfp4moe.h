@@ -32,8 +32,10 @@
  *                             nibble = E2M1 code (bit 3 sign; magnitudes
  *                             0, .5, 1, 1.5, 2, 3, 4, 6)
  *   scales  [N, K/16]         one block scale per 16 consecutive K elements:
- *                             uint8 FP8-E4M3 (NVFP4_SCALE_E4M3) or uint16
- *                             IEEE binary16 (NVFP4_SCALE_FP16)
+ *                             uint8 FP8-E4M3 (NVFP4_SCALE_E4M3), uint16
+ *                             IEEE binary16 (NVFP4_SCALE_FP16) or fp32
+ *                             (NVFP4_SCALE_FP32); or [N, K/32] uint8 E8M0, one
+ *                             per 32 elements (NVFP4_SCALE_UE8M0)
  *   tensor_scale  one fp32    W[n,k] = E2M1 * block_scale * tensor_scale
  *
  * Conventions for every call
@@ -83,9 +85,18 @@ typedef enum {
     NVFP4_ERR_ARCH = 8                /* the current device is not sm_103           */
 } nvfp4_status;
 
+/* Block-scale contract of an NVFP4 matrix (the tag travels with every matrix and layer;
+ * a call that cannot consume a kind refuses it, nothing is reinterpreted):
+ *   E4M3   FP8-E4M3 scale per 16 elements, fp32 tensor scale  (the workload's format)
+ *   FP16   IEEE binary16 scale per 16 elements, tensor scale 1 (README P1 stage)
+ *   FP32   fp32 scale per 16 elements, tensor scale 1          (README P52: Lynn-native)
+ *   UE8M0  power-of-two E8M0 scale 2^(b-127) per 32 elements, tensor scale 1
+ *          (README P17/P18: the vendor MX layout, neutral byte 127)                   */
 typedef enum {
     NVFP4_SCALE_E4M3 = 0,
-    NVFP4_SCALE_FP16 = 1
+    NVFP4_SCALE_FP16 = 1,
+    NVFP4_SCALE_FP32 = 2,
+    NVFP4_SCALE_UE8M0 = 3
 } nvfp4_scale_kind;
 
 /* One NVFP4 matrix W[N,K] (device pointers; see the storage section above). */
@@ -239,6 +250,32 @@ NVFP4_API nvfp4_status moe_layer_forward(const moe_layer_desc* d, const uint16_t
 NVFP4_API size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T);
 
 /*
+ * moe_layer_forward_residual - the layer inside a decoder block's residual stream, with
+ * the pre-MoE norm fused in:
+ *   x      = bf16( h / sqrt(mean_i h[t,i]^2 + eps) * (1 + norm_w) )   (RMSNorm, (1 + w) form)
+ *   h_out  = bf16( h + moe_layer(x) )                                (one rounding)
+ *   Defined by: lynn-engine tutorials index, row 01 (RMSNorm = (1.0 + weight) x x_norm)
+ *   and the Qwen 3.6 config block (rms_norm (1.0 + weight) x x_norm); Lynn Engine
+ *   write-up, "Fused Kernels" (fused RMSNorm) and the README's decode launch-overhead
+ *   campaign (fused RMSNorm cut launches per token).
+ *   norm_w        bf16 [H] device;  eps >= 0 (Qwen's value is 1e-6)
+ *   h             bf16 [T, H] device, the residual stream;  h_out bf16 [T, H] device
+ *                 (written; may be the same buffer as h)
+ *   topk_ids_out, topk_w_out, workspace, stream: as for moe_layer_forward, with
+ *   workspace >= moe_layer_residual_workspace_size(d, T) bytes (the layer's scratch,
+ *   then the normalised rows), zeroed once with nvfp4_workspace_init.
+ *   The single-token kernel computes the norm inside its activation staging and adds h
+ *   in its output epilogue (still one launch); the other paths run one norm kernel
+ *   first and add h in their combine epilogues. The norm is computed in fp32 (sum of
+ *   squares in a fixed order, IEEE square root and division).
+ */
+NVFP4_API nvfp4_status moe_layer_forward_residual(const moe_layer_desc* d, const uint16_t* norm_w, float eps,
+                                                  const uint16_t* h, int32_t T, uint16_t* h_out,
+                                                  int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                                  size_t workspace_bytes, void* stream);
+NVFP4_API size_t moe_layer_residual_workspace_size(const moe_layer_desc* d, int32_t T);
+
+/*
  * moe_layer_forward_noalloc - the same layer as moe_layer_forward, for callers
  * that cannot allocate device memory where they run the layer (a host callback,
  * a plugin whose host framework owns all device allocations, a process whose
@@ -261,6 +298,24 @@ NVFP4_API size_t moe_layer_workspace_size(const moe_layer_desc* d, int32_t T);
 NVFP4_API nvfp4_status moe_layer_forward_noalloc(const moe_layer_desc* d, const uint16_t* x, int32_t T,
                                                  uint16_t* y, int32_t* topk_ids_out, float* topk_w_out,
                                                  void* stream);
+
+/*
+ * nvfp4_scale_kind_of - which block-scale contract a stored NVFP4 matrix uses, from its
+ * metadata alone (no tensor is read), so that a matrix is never consumed under the wrong
+ * contract.
+ *   Defined by: lynn-engine README, P59 note (a metadata-only NVFP4 layout classifier that
+ *   tells the Lynn-native per-16 layout from vendor layouts before any tensor is loaded;
+ *   every cross mis-load fails loud).
+ *   N, K              the matrix shape (K % 16 == 0)
+ *   scale_count       number of scale elements stored for the matrix
+ *   scale_elem_bytes  bytes per scale element (1, 2 or 4)
+ *   kind_out          host pointer, receives the nvfp4_scale_kind
+ *   Returns NVFP4_OK, or NVFP4_ERR_INVALID_ARG when the metadata match no contract (for
+ *   example a per-32 count with 2-byte elements, or a count that fits neither block size).
+ *   Host only; enqueues nothing.
+ */
+NVFP4_API nvfp4_status nvfp4_scale_kind_of(int32_t N, int32_t K, size_t scale_count, int32_t scale_elem_bytes,
+                                           int32_t* kind_out);
 
 /* Zero a workspace (enqueued on `stream`). Needed once before first use, and
  * again after a call reported NVFP4_ERR_DEVICE_TIMEOUT or a CUDA error (a call

@@ -23,18 +23,28 @@ LIB_PATH = os.path.join(HERE, "libnvfp4moe.so")
 
 SCALE_E4M3 = 0
 SCALE_FP16 = 1
+SCALE_FP32 = 2     # fp32 scale per 16 elements
+SCALE_UE8M0 = 3    # E8M0 power-of-two scale per 32 elements
+
+
+def scale_shape(rows: int, K: int, kind: int):
+    """(shape, dtype) of the block scales of a [rows, K] matrix of the given kind."""
+    if kind == SCALE_UE8M0:
+        return (rows, K // 32), torch.uint8
+    return (rows, K // 16), {SCALE_E4M3: torch.uint8, SCALE_FP16: torch.int16, SCALE_FP32: torch.float32}[kind]
 
 
 def launches_per_layer_call(T: int, H: int = 2048, kind: int = 0, shared: bool = True, E: int = 256,
-                            I: int = 512, Is: int = 512) -> int:
+                            I: int = 512, Is: int = 512, k: int = 8) -> int:
     """Kernel launches one moe_layer_forward call enqueues (routing outputs not requested):
-    one for the single-token fused kernel; four for the tensor-core multi-token decode
+    one for the single-token fused kernel (E4M3 or FP16 scales); four for the tensor-core multi-token decode
     path (router + route, gate/up, down, combine; E4M3 scales, H, I, Is multiples of
     256 and at most 4096); five for the other multi-token shapes (router, top-k, lists,
     gate/up, down), per 64-token chunk for FP16-scaled layers above 64 tokens; and for
     the prefill path router (and the sum of its K-split partials), gate, top-k, three
     list passes, gate/up, down and combine (no gate launch without a shared expert)."""
-    if T == 1 and H % 256 == 0 and H <= 2048:
+    if (T == 1 and kind in (SCALE_E4M3, SCALE_FP16) and H % 256 == 0 and I % 256 == 0 and Is % 256 == 0
+            and Is <= I and H <= 4096 and I <= 4096 and k * I + Is <= 8192):
         return 1
     mma = (kind == 0 and H % 256 == 0 and I % 256 == 0 and Is % 256 == 0 and
            H <= 4096 and I <= 4096 and Is <= 4096)
@@ -103,6 +113,13 @@ lib.moe_layer_forward.restype = _i32
 lib.moe_layer_forward.argtypes = [ctypes.POINTER(MoELayerDescC), _P, _i32, _P, _P, _P, _P, _sz, _P]
 lib.moe_layer_workspace_size.restype = _sz
 lib.moe_layer_workspace_size.argtypes = [ctypes.POINTER(MoELayerDescC), _i32]
+lib.nvfp4_scale_kind_of.restype = _i32
+lib.nvfp4_scale_kind_of.argtypes = [_i32, _i32, _sz, _i32, ctypes.POINTER(_i32)]
+lib.moe_layer_forward_residual.restype = _i32
+lib.moe_layer_forward_residual.argtypes = [ctypes.POINTER(MoELayerDescC), _P, ctypes.c_float, _P, _i32, _P, _P, _P,
+                                           _P, _sz, _P]
+lib.moe_layer_residual_workspace_size.restype = _sz
+lib.moe_layer_residual_workspace_size.argtypes = [ctypes.POINTER(MoELayerDescC), _i32]
 lib.nvfp4_workspace_init.restype = _i32
 lib.nvfp4_workspace_init.argtypes = [_P, _sz, _P]
 lib.nvfp4_get_device_status.restype = _i32
@@ -189,9 +206,9 @@ def nvfp4_pack(w: torch.Tensor, kind: int = SCALE_E4M3, out: Optional[NVFP4Weigh
     assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous() and w.dim() == 2
     N, K = w.shape
     if out is None:
-        sdt = torch.uint8 if kind == SCALE_E4M3 else torch.int16
+        sshape, sdt = scale_shape(N, K, kind)
         out = NVFP4Weight(torch.empty(N, K // 2, dtype=torch.uint8, device=w.device),
-                          torch.empty(N, K // 16, dtype=sdt, device=w.device),
+                          torch.empty(*sshape, dtype=sdt, device=w.device),
                           torch.empty(1, dtype=torch.float32, device=w.device), N, K, kind)
     ws = ws or _pack_ws(w.device)
     _check(lib.nvfp4_pack(_ptr(w), N, K, kind, _ptr(out.packed), _ptr(out.scales), _ptr(out.tensor_scale),
@@ -209,6 +226,15 @@ def nvfp4_pack_into(w: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     ws = ws or _pack_ws(w.device)
     _check(lib.nvfp4_pack(_ptr(w), N, K, kind, _ptr(packed), _ptr(scales), _ptr(tensor_scale),
                           ws.ptr(), ws.nbytes, _stream(stream)), "nvfp4_pack")
+
+
+def nvfp4_scale_kind_of(N: int, K: int, scales) -> int:
+    """The scale contract of an [N, K] NVFP4 matrix from its scale tensor's metadata (element
+    count and size); raises NVFP4Error when it matches none."""
+    out = _i32(-1)
+    _check(lib.nvfp4_scale_kind_of(N, K, scales.numel(), scales.element_size(), ctypes.byref(out)),
+           "nvfp4_scale_kind_of")
+    return out.value
 
 
 # ---------------------------------------------------------------- GEMV
@@ -269,22 +295,24 @@ class MoELayer:
 
     @staticmethod
     def allocate(H, E, k, I, Is, kind=SCALE_E4M3, device="cuda") -> "MoELayer":
-        sdt = torch.uint8 if kind == SCALE_E4M3 else torch.int16
         z = dict(device=device)
+        (_, gcols), sdt = scale_shape(1, H, kind)
+        (_, dcols), _ = scale_shape(1, I, kind)
         L = MoELayer(H, E, k, I, Is, kind,
                      torch.empty(E, H, dtype=torch.bfloat16, **z),
                      torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, **z),
-                     torch.empty(E, 2 * I, H // 16, dtype=sdt, **z),
+                     torch.empty(E, 2 * I, gcols, dtype=sdt, **z),
                      torch.empty(E, 2, dtype=torch.float32, **z),
                      torch.empty(E, H, I // 2, dtype=torch.uint8, **z),
-                     torch.empty(E, H, I // 16, dtype=sdt, **z),
+                     torch.empty(E, H, dcols, dtype=sdt, **z),
                      torch.empty(E, dtype=torch.float32, **z))
         if Is > 0:
+            (_, scols), _ = scale_shape(1, Is, kind)
             L.sh_gu_packed = torch.empty(2 * Is, H // 2, dtype=torch.uint8, **z)
-            L.sh_gu_scales = torch.empty(2 * Is, H // 16, dtype=sdt, **z)
+            L.sh_gu_scales = torch.empty(2 * Is, gcols, dtype=sdt, **z)
             L.sh_gu_tscale = torch.empty(4, dtype=torch.float32, **z)   # 2 used, 16-byte aligned
             L.sh_dn_packed = torch.empty(H, Is // 2, dtype=torch.uint8, **z)
-            L.sh_dn_scales = torch.empty(H, Is // 16, dtype=sdt, **z)
+            L.sh_dn_scales = torch.empty(H, scols, dtype=sdt, **z)
             L.sh_dn_tscale = torch.empty(4, dtype=torch.float32, **z)
             L.sh_gate_w = torch.empty(H, dtype=torch.bfloat16, **z)
         return L
@@ -320,9 +348,11 @@ class MoELayer:
         return d
 
     def weight_bytes_per_expert(self) -> int:
-        sb = 1 if self.kind == SCALE_E4M3 else 2
         H, I = self.H, self.I
-        return 2 * I * H // 2 + 2 * I * H // 16 * sb + H * I // 2 + H * I // 16 * sb + 12
+        (_, gc), gdt = scale_shape(1, H, self.kind)
+        (_, dc), _ = scale_shape(1, I, self.kind)
+        sb = torch.tensor([], dtype=gdt).element_size()
+        return 2 * I * H // 2 + 2 * I * gc * sb + H * I // 2 + H * dc * sb + 12
 
 
 def moe_layer_workspace_size(layer: MoELayer, T: int) -> int:
@@ -350,6 +380,30 @@ def moe_layer_forward(layer: MoELayer, x: torch.Tensor, ws: Optional[Workspace] 
     if want_route:
         return y, ids_out, w_out
     return y
+
+
+def moe_layer_forward_residual(layer: MoELayer, h: torch.Tensor, norm_w: torch.Tensor, eps: float = 1e-6,
+                               ws: Optional[Workspace] = None, h_out: Optional[torch.Tensor] = None,
+                               want_route: bool = False, stream=None, desc: Optional[MoELayerDescC] = None):
+    """h_out = h + layer(RMSNorm_(1+w)(h)) [T, H] bf16 (and optionally the routing) for the
+    residual stream h [T, H] bf16; h_out may be h itself."""
+    h = _u16(h)
+    T = h.shape[0]
+    d = desc if desc is not None else layer.desc()
+    if ws is None:
+        ws = Workspace(lib.moe_layer_residual_workspace_size(ctypes.byref(d), T), device=h.device, stream=stream)
+    if h_out is None:
+        h_out = torch.empty(T, layer.H, dtype=torch.bfloat16, device=h.device)
+    ids_out = w_out = None
+    if want_route:
+        ids_out = torch.empty(T, layer.k, dtype=torch.int32, device=h.device)
+        w_out = torch.empty(T, layer.k, dtype=torch.float32, device=h.device)
+    _check(lib.moe_layer_forward_residual(ctypes.byref(d), _ptr(_u16(norm_w)), float(eps), _ptr(h), T, _ptr(h_out),
+                                          _ptr(ids_out), _ptr(w_out), ws.ptr(), ws.nbytes, _stream(stream)),
+           "moe_layer_forward_residual")
+    if want_route:
+        return h_out, ids_out, w_out
+    return h_out
 
 
 def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, y: Optional[torch.Tensor] = None,

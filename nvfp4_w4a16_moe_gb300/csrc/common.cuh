@@ -80,13 +80,53 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
     return f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
 }
 
-// Decoded block scale of block `i` of a scale row (E4M3 bytes or FP16 halves).
+// E8M0 byte -> 2^(b - 127) (exact; 0xFF is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    b &= 0xFFu;
+    if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+    if (b == 0u) return __uint_as_float(0x00400000u);   // 2^-127, an fp32 subnormal
+    return __uint_as_float(b << 23);
+}
+
+// Bytes of one row of block scales for K elements: E4M3 and FP16 one scale per 16
+// elements (1 and 2 bytes), FP32 one per 16 (4 bytes), UE8M0 one per 32 (1 byte).
+__host__ __device__ constexpr size_t scale_row_bytes_of(int kind, size_t K) {
+    return kind == NVFP4_SCALE_E4M3 ? K / 16 : kind == NVFP4_SCALE_FP16 ? K / 8
+         : kind == NVFP4_SCALE_FP32 ? K / 4 : K / 32;
+}
+
+// The two block scales of 32-element segment s of a scale row (for UE8M0 the segment is
+// one block, so both are the same value).
+template <int KIND>
+__device__ __forceinline__ void seg_scales(const uint8_t* srow, int s, float& s0, float& s1) {
+    if constexpr (KIND == NVFP4_SCALE_E4M3) {
+        const uint32_t b = *reinterpret_cast<const uint16_t*>(srow + 2 * s);
+        s0 = e4m3_to_f32(b & 0xFFu);
+        s1 = e4m3_to_f32(b >> 8);
+    } else if constexpr (KIND == NVFP4_SCALE_FP16) {
+        const uint32_t h = *reinterpret_cast<const uint32_t*>(srow + 4 * s);
+        s0 = f16_bits_to_f32(static_cast<uint16_t>(h & 0xFFFFu));
+        s1 = f16_bits_to_f32(static_cast<uint16_t>(h >> 16));
+    } else if constexpr (KIND == NVFP4_SCALE_FP32) {
+        const float2 f = *reinterpret_cast<const float2*>(srow + 8 * s);
+        s0 = f.x;
+        s1 = f.y;
+    } else {
+        s0 = s1 = e8m0_to_f32(srow[s]);
+    }
+}
+
+// Decoded block scale of block `i` of a scale row (16-element blocks; UE8M0: block i / 2).
 template <int KIND>
 __device__ __forceinline__ float scale_at(const void* row, int i) {
     if constexpr (KIND == NVFP4_SCALE_E4M3) {
         return e4m3_to_f32(static_cast<const uint8_t*>(row)[i]);
-    } else {
+    } else if constexpr (KIND == NVFP4_SCALE_FP16) {
         return f16_bits_to_f32(static_cast<const uint16_t*>(row)[i]);
+    } else if constexpr (KIND == NVFP4_SCALE_FP32) {
+        return static_cast<const float*>(row)[i];
+    } else {
+        return e8m0_to_f32(static_cast<const uint8_t*>(row)[i >> 1]);
     }
 }
 

@@ -559,7 +559,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
 // y[t, n] = bf16( sum_j P[t*k + j, n]  (j = 0..k-1)  + Ps[t, n] ), that order.
 __global__ void __launch_bounds__(kThreads)
 combine_mt_kernel(const float* __restrict__ P, const float* __restrict__ Ps, int T, int H, int k,
-                  uint16_t* __restrict__ y) {
+                  const uint16_t* __restrict__ resid, uint16_t* __restrict__ y) {
     const int q4 = H >> 2;
     const int i = blockIdx.x * kThreads + threadIdx.x;
     if (i >= T * q4) return;
@@ -576,6 +576,10 @@ combine_mt_kernel(const float* __restrict__ P, const float* __restrict__ Ps, int
     if (Ps) {
         const float4 v = *reinterpret_cast<const float4*>(Ps + (size_t)t * H + 4 * c);
         a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    if (resid) {   // the residual stream, added before the one rounding
+        const uint2 r = *reinterpret_cast<const uint2*>(resid + (size_t)t * H + 4 * c);
+        a.x += bf16lo(r.x); a.y += bf16hi(r.x); a.z += bf16lo(r.y); a.w += bf16hi(r.y);
     }
     uint2 o;
     o.x = (uint32_t)f32_to_bf16(a.x) | ((uint32_t)f32_to_bf16(a.y) << 16);
@@ -598,7 +602,7 @@ bool decode_mma_supported(const moe_layer_desc& d, int T) {
 
 cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                   int32_t* ids_out, float* w_out, const LayerWs& ws, const DeviceInfo& dev,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const uint16_t* resid) {
     cudaError_t err;
     const bool shared = d.Is > 0;
     const int passes_shared = (T + kPass - 1) / kPass;
@@ -646,7 +650,7 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
     }
     {   // 5. combine
         const int n = T * (d.H / 4);
-        combine_mt_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, s>>>(P, Ps, T, d.H, d.k, y);
+        combine_mt_kernel<<<(n + kThreads - 1) / kThreads, kThreads, 0, s>>>(P, Ps, T, d.H, d.k, resid, y);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     return cudaSuccess;

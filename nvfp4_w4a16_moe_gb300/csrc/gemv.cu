@@ -71,7 +71,7 @@ struct GemvParams {
     int N, K, T;
     int ngroups;              // ceil(N / 8)
     int slots;                // ring depth
-    uint32_t slot_bytes;      // kCRows * (K/2 + K/16 * sb)
+    uint32_t slot_bytes;      // kCRows * (K/2 + scale row bytes)
     uint32_t off_ring;        // shared-memory offset of the ring (after the x stage)
 };
 
@@ -113,19 +113,6 @@ __device__ __forceinline__ int gemv_row_shift(uint32_t bf16_amax) {
     return min(126, max(-126, 14 - e));
 }
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
-
-template <int KIND>
-__device__ __forceinline__ void scale_pair(const uint8_t* srow, int s, float& s0, float& s1) {
-    if constexpr (KIND == NVFP4_SCALE_E4M3) {
-        const uint32_t b2 = *reinterpret_cast<const uint16_t*>(srow + 2 * s);
-        s0 = e4m3_to_f32(b2 & 0xFFu);
-        s1 = e4m3_to_f32(b2 >> 8);
-    } else {
-        const uint32_t h2 = *reinterpret_cast<const uint32_t*>(srow + 4 * s);
-        s0 = f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFFu));
-        s1 = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
-    }
-}
 
 // One 16-byte segment (32 codes) of two rows against one token's activations: the
 // activation units are loaded once for both rows; eight independent accumulators.
@@ -188,8 +175,7 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
     const int nc = g1 - g0;                        // chunks per pass
     const int passes = (T + TC - 1) / TC;
     const int nv = nc * passes;                    // chunks streamed by this CTA
-    const int sb = KIND == NVFP4_SCALE_E4M3 ? 1 : 2;
-    const uint32_t rowB = (uint32_t)K >> 1, srowB = (uint32_t)(K >> 4) * sb;
+    const uint32_t rowB = (uint32_t)K >> 1, srowB = (uint32_t)scale_row_bytes_of(KIND, K);
     const uint32_t off_sc = kCRows * rowB;         // scale bytes inside a slot
     const int nseg = K >> 5, nunit = K >> 3;
     uint8_t* ring = gsm + p.off_ring;
@@ -337,8 +323,8 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                         const uint4 wa = reinterpret_cast<const uint4*>(rowa)[s];
                         const uint4 wb = reinterpret_cast<const uint4*>(rowb)[s];
                         float a0, a1, b0, b1;
-                        scale_pair<KIND>(sra, s, a0, a1);
-                        scale_pair<KIND>(srb, s, b0, b1);
+                        seg_scales<KIND>(sra, s, a0, a1);
+                        seg_scales<KIND>(srb, s, b0, b1);
                         uint32_t qa[16], qb[16];
                         expand_seg(wa, qa);
                         expand_seg(wb, qb);
@@ -372,7 +358,7 @@ struct GemvPlan {
 GemvPlan plan_gemv(const nvfp4_weight& W, int T, const DeviceInfo& dev) {
     GemvPlan g;
     const int K = W.K, N = W.N;
-    const uint32_t sb = W.kind == NVFP4_SCALE_E4M3 ? 1 : 2;
+    const uint32_t srow = (uint32_t)scale_row_bytes_of(W.kind, W.K);
     g.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
     if (T == 3) g.tc = 4;
     if (T >= 5 && T < 8) g.tc = 8;
@@ -380,7 +366,7 @@ GemvPlan plan_gemv(const nvfp4_weight& W, int T, const DeviceInfo& dev) {
     g.grid = ngroups < dev.num_sms ? ngroups : dev.num_sms;
     const int nc_max = (ngroups + g.grid - 1) / g.grid;
     const int passes = (T + g.tc - 1) / g.tc;
-    g.slot_bytes = (uint32_t)kCRows * ((uint32_t)K / 2 + (uint32_t)K / 16 * sb);
+    g.slot_bytes = (uint32_t)kCRows * ((uint32_t)K / 2 + srow);
     g.off_ring = (uint32_t)g.tc * (uint32_t)K * 2u;
     // two CTAs per SM when the ring and stage fit in ~100 KB (the next launch's
     // weight prologue then overlaps this one under programmatic dependent launch)
@@ -451,8 +437,13 @@ cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_
     P.slots = g.slots;
     P.slot_bytes = g.slot_bytes;
     P.off_ring = g.off_ring;
-    cudaError_t err = W.kind == NVFP4_SCALE_E4M3 ? launch_kind<NVFP4_SCALE_E4M3>(P, g, dev, s)
-                                                 : launch_kind<NVFP4_SCALE_FP16>(P, g, dev, s);
+    cudaError_t err;
+    switch (W.kind) {
+        case NVFP4_SCALE_E4M3: err = launch_kind<NVFP4_SCALE_E4M3>(P, g, dev, s); break;
+        case NVFP4_SCALE_FP16: err = launch_kind<NVFP4_SCALE_FP16>(P, g, dev, s); break;
+        case NVFP4_SCALE_FP32: err = launch_kind<NVFP4_SCALE_FP32>(P, g, dev, s); break;
+        default: err = launch_kind<NVFP4_SCALE_UE8M0>(P, g, dev, s); break;
+    }
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -27,6 +27,16 @@ cudaError_t launch_route_lists(const int32_t* ids, int total, int E, int32_t* of
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                          int32_t* offsets, int32_t* token_list, cudaStream_t s);
 
+// Exchange words of the one-launch single-token kernel: kWordReplicas copies of the E + 1
+// logits (8-byte words, each copy padded to 16 words) and of the k*I + Is SwiGLU values
+// (4-byte words, each copy padded to 32 words); in 8-byte units.
+constexpr int kWordReplicas = 8;
+__host__ __device__ inline size_t t1_logit_stride(const moe_layer_desc& d) { return ((size_t)d.E + 1 + 15) & ~size_t(15); }
+__host__ __device__ inline size_t t1_h_stride(const moe_layer_desc& d) { return ((size_t)d.k * d.I + d.Is + 31) & ~size_t(31); }
+__host__ __device__ inline size_t t1_words(const moe_layer_desc& d) {
+    return (size_t)kWordReplicas * (t1_logit_stride(d) + t1_h_stride(d) / 2);
+}
+
 // Workspace of one layer call (device scratch carved from the caller's buffer).
 struct LayerWs {
     WsHeader* hdr;
@@ -39,7 +49,7 @@ struct LayerWs {
     int32_t* active;      // [E + 1]    active[0] = A, active[1..A] = expert ids ascending
     float* h;             // [T * k, I] routed SwiGLU intermediates (entry-major)
     float* hs;            // [T, Is]    shared intermediates
-    unsigned long long* words;  // [E + 2 + k*I + Is] (launch tag, value) words of the one-launch kernel
+    unsigned long long* words;  // [t1_words(d)] (launch tag, value) words of the one-launch kernel
     int32_t* pass_map;    // [E + T*k + 2]  pass_map[0] = P, then (active slot << 8) | pass
     float* part;          // [T*k + T, H]  weighted routed rows, then the shared rows
     uint32_t* amax;       // [T + T*k + T] max |x| of each token, then max |h| of each h row (fp32 bits)
@@ -49,21 +59,29 @@ struct LayerWs {
 LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T);
 size_t layer_ws_bytes(const moe_layer_desc& d, int T);
 
+// resid (nullable, bf16 [T, H]): added to every output element before its one rounding
 cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                               int32_t* ids_out, float* w_out, const LayerWs& ws,
-                              const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
+                              const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s,
+                              const uint16_t* resid = nullptr);
 
 // Multi-token decode on mma.sync (E4M3 scales, H, I, Is multiples of 256, <= 4096).
 bool decode_mma_supported(const moe_layer_desc& d, int T);
 cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                   int32_t* ids_out, float* w_out, const LayerWs& ws, const DeviceInfo& dev,
-                                  cudaStream_t s);
+                                  cudaStream_t s, const uint16_t* resid = nullptr);
 
 // One-launch single-token decode (persistent grid, two bounded grid barriers).
 bool fused_decode_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev);
 cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, uint16_t* y,
                                     int32_t* ids_out, float* w_out, const LayerWs& ws,
-                                    const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s);
+                                    const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s,
+                                    const uint16_t* norm_w = nullptr, float eps = 0.f,
+                                    const uint16_t* resid = nullptr);
+
+// Pre-MoE RMSNorm, (1 + w) form: out[t] = bf16(h[t] / sqrt(mean(h[t]^2) + eps) * (1 + w)).
+cudaError_t launch_rmsnorm(const uint16_t* h, int T, int H, const uint16_t* w, float eps, uint16_t* out,
+                           cudaStream_t s);
 
 // Prefill path (T > 64 tokens, E4M3 scales): grouped tensor-core GEMMs.
 constexpr int kTokTile = 256;   // token rows per grouped-GEMM tile
@@ -111,7 +129,8 @@ PrefillWs carve_prefill_ws(void* base, const moe_layer_desc& d, int T);
 int prefill_launch_count(const moe_layer_desc& d, int T);
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
-                               cudaStream_t s);
+                               cudaStream_t s,
+                               const uint16_t* resid = nullptr);
 // Grouped tcgen05 GEMM over the token tiles of every slot: mode 0 = gate/up with the
 // SwiGLU epilogue (x -> h, hs), mode 1 = down with the weighted epilogue (h, hs -> Y).
 cudaError_t launch_grouped_tc(const GroupedParams& P, int mode, int tiles_max, WsHeader* hdr,

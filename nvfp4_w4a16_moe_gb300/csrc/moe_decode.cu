@@ -105,15 +105,7 @@ struct SlotInfo {
 
 template <int KIND>
 __device__ __forceinline__ void scales2(const uint8_t* srow, int s, float& s0, float& s1) {
-    if constexpr (KIND == NVFP4_SCALE_E4M3) {
-        const uint32_t b2 = *reinterpret_cast<const uint16_t*>(srow + 2 * s);
-        s0 = e4m3_to_f32(b2 & 0xFF);
-        s1 = e4m3_to_f32(b2 >> 8);
-    } else {
-        const uint32_t h2 = *reinterpret_cast<const uint32_t*>(srow + 4 * s);
-        s0 = f16_bits_to_f32(static_cast<uint16_t>(h2 & 0xFFFF));
-        s1 = f16_bits_to_f32(static_cast<uint16_t>(h2 >> 16));
-    }
+    seg_scales<KIND>(srow, s, s0, s1);
 }
 
 // x[t] (bf16) for the chunk's tokens -> xs[tt][c][s][4] fp32 (segment-interleaved)
@@ -162,7 +154,7 @@ gateup_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T, const int
     __shared__ int ent[kGuTc];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = d.H, nseg = H >> 5;
-    const int sb = KIND == NVFP4_SCALE_E4M3 ? 1 : 2;
+    constexpr int kind = KIND;
     const int A = active[0];
     const int ib_r = (d.I + kPairRows - 1) / kPairRows;
     const int ib_s = d.Is > 0 ? (d.Is + kPairRows - 1) / kPairRows : 0;
@@ -176,7 +168,7 @@ gateup_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T, const int
             const int e = active[1 + slot];
             si.Irows = d.I;
             si.packed = d.gu_packed + (size_t)e * 2 * d.I * (H / 2);
-            si.scales = static_cast<const uint8_t*>(d.gu_scales) + (size_t)e * 2 * d.I * (H / 16) * sb;
+            si.scales = static_cast<const uint8_t*>(d.gu_scales) + (size_t)e * 2 * d.I * scale_row_bytes_of(kind, H);
             si.ts_g = __ldg(d.gu_tscale + 2 * e);
             si.ts_u = __ldg(d.gu_tscale + 2 * e + 1);
             si.list = token_list + offsets[e];
@@ -210,8 +202,8 @@ gateup_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T, const int
                 if (i >= Ir) break;
                 const uint8_t* grow = si.packed + (size_t)i * (H / 2);
                 const uint8_t* urow = si.packed + (size_t)(Ir + i) * (H / 2);
-                const uint8_t* gsc = si.scales + (size_t)i * (H / 16) * sb;
-                const uint8_t* usc = si.scales + (size_t)(Ir + i) * (H / 16) * sb;
+                const uint8_t* gsc = si.scales + (size_t)i * scale_row_bytes_of(kind, H);
+                const uint8_t* usc = si.scales + (size_t)(Ir + i) * scale_row_bytes_of(kind, H);
                 float ga[kGuTc], ua[kGuTc];
 #pragma unroll
                 for (int t = 0; t < kGuTc; ++t) { ga[t] = 0.f; ua[t] = 0.f; }
@@ -260,10 +252,10 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads)
 down_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ ids, const float* __restrict__ wts,
             const float* __restrict__ gate_logit, const float* __restrict__ h,
-            const float* __restrict__ hs, uint16_t* __restrict__ y) {
+            const float* __restrict__ hs, const uint16_t* __restrict__ resid, uint16_t* __restrict__ y) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = d.H, I = d.I, Is = d.Is, k = d.k;
-    const int sb = KIND == NVFP4_SCALE_E4M3 ? 1 : 2;
+    constexpr int kind = KIND;
     const int nseg_r = I >> 5, nseg_s = Is >> 5;
     const int work_r = k * nseg_r;
     const int work = work_r + nseg_s;
@@ -277,7 +269,7 @@ down_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ ids, const floa
                 const int j = p / nseg_r, s = p - j * nseg_r;
                 const int e = ids[t * k + j];
                 const uint8_t* row = d.dn_packed + ((size_t)e * H + n) * (I / 2);
-                const uint8_t* srow = static_cast<const uint8_t*>(d.dn_scales) + ((size_t)e * H + n) * (I / 16) * sb;
+                const uint8_t* srow = static_cast<const uint8_t*>(d.dn_scales) + ((size_t)e * H + n) * scale_row_bytes_of(kind, I);
                 const uint4 wv = *reinterpret_cast<const uint4*>(row + 16 * (size_t)s);
                 float s0, s1;
                 scales2<KIND>(srow, s, s0, s1);
@@ -301,7 +293,7 @@ down_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ ids, const floa
             } else {
                 const int s = p - work_r;
                 const uint8_t* row = d.sh_dn_packed + (size_t)n * (Is / 2);
-                const uint8_t* srow = static_cast<const uint8_t*>(d.sh_dn_scales) + (size_t)n * (Is / 16) * sb;
+                const uint8_t* srow = static_cast<const uint8_t*>(d.sh_dn_scales) + (size_t)n * scale_row_bytes_of(kind, Is);
                 const uint4 wv = *reinterpret_cast<const uint4*>(row + 16 * (size_t)s);
                 float s0, s1;
                 scales2<KIND>(srow, s, s0, s1);
@@ -329,6 +321,7 @@ down_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ ids, const floa
         if (lane == 0) {
             float v = acc_r;
             if (Is > 0) v = fmaf(sigmoid_f32(gate_logit[t]) * __ldg(d.sh_dn_tscale), acc_s, v);
+            if (resid) v += bf16_to_f32(resid[(size_t)t * H + n]);   // residual stream, before the rounding
             y[(size_t)t * H + n] = f32_to_bf16(v);
         }
     }
@@ -357,7 +350,7 @@ size_t layer_ws_bytes(const moe_layer_desc& d, int T) {
     b += align256(sizeof(int32_t) * (size_t)(d.E + 1));
     b += align256(sizeof(float) * Tk * d.I);
     b += align256(sizeof(float) * (size_t)T * d.Is);
-    b += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
+    b += align256(sizeof(unsigned long long) * t1_words(d));
     b += align256(sizeof(int32_t) * (Tk + d.E + 2));
     b += align256(sizeof(float) * (Tk + T) * d.H);
     b += align256(sizeof(uint32_t) * (Tk + 2 * (size_t)T));
@@ -379,7 +372,7 @@ LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T) {
     w.h = reinterpret_cast<float*>(p); p += align256(sizeof(float) * Tk * d.I);
     w.hs = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (size_t)T * d.Is);
     w.words = reinterpret_cast<unsigned long long*>(p);
-    p += align256(sizeof(unsigned long long) * (size_t)(d.E + 2 + d.k * d.I + d.Is));
+    p += align256(sizeof(unsigned long long) * t1_words(d));
     w.pass_map = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * (Tk + d.E + 2));
     w.part = reinterpret_cast<float*>(p); p += align256(sizeof(float) * (Tk + T) * d.H);
     w.amax = reinterpret_cast<uint32_t*>(p); p += align256(sizeof(uint32_t) * (Tk + 2 * (size_t)T));
@@ -390,7 +383,7 @@ LayerWs carve_layer_ws(void* base, const moe_layer_desc& d, int T) {
 template <int KIND>
 static cudaError_t decode_impl(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                int32_t* ids_out, float* w_out, const LayerWs& ws,
-                               const DeviceInfo& dev, cudaStream_t s) {
+                               const DeviceInfo& dev, cudaStream_t s, const uint16_t* resid) {
     cudaError_t err;
     // 1. router GEMV (+ shared gate pre-activation)
     {
@@ -426,7 +419,7 @@ static cudaError_t decode_impl(const moe_layer_desc& d, const uint16_t* x, int T
         const long items = (long)d.H * T;
         long grid = (items + kWarps - 1) / kWarps;
         if (grid > dev.num_sms * 4) grid = dev.num_sms * 4;
-        down_kernel<KIND><<<(int)grid, kThreads, 0, s>>>(d, T, ws.ids, ws.w, ws.gate_logit, ws.h, ws.hs, y);
+        down_kernel<KIND><<<(int)grid, kThreads, 0, s>>>(d, T, ws.ids, ws.w, ws.gate_logit, ws.h, ws.hs, resid, y);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (ids_out || w_out) {
@@ -439,11 +432,16 @@ static cudaError_t decode_impl(const moe_layer_desc& d, const uint16_t* x, int T
 
 cudaError_t launch_moe_decode(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                               int32_t* ids_out, float* w_out, const LayerWs& ws,
-                              const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s) {
+                              const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s,
+                              const uint16_t* resid) {
     (void)wait_limit;
-    if (decode_mma_supported(d, T)) return launch_moe_decode_mma(d, x, T, y, ids_out, w_out, ws, dev, s);
-    if (d.kind == NVFP4_SCALE_E4M3) return decode_impl<NVFP4_SCALE_E4M3>(d, x, T, y, ids_out, w_out, ws, dev, s);
-    return decode_impl<NVFP4_SCALE_FP16>(d, x, T, y, ids_out, w_out, ws, dev, s);
+    if (decode_mma_supported(d, T)) return launch_moe_decode_mma(d, x, T, y, ids_out, w_out, ws, dev, s, resid);
+    switch (d.kind) {
+        case NVFP4_SCALE_E4M3: return decode_impl<NVFP4_SCALE_E4M3>(d, x, T, y, ids_out, w_out, ws, dev, s, resid);
+        case NVFP4_SCALE_FP16: return decode_impl<NVFP4_SCALE_FP16>(d, x, T, y, ids_out, w_out, ws, dev, s, resid);
+        case NVFP4_SCALE_FP32: return decode_impl<NVFP4_SCALE_FP32>(d, x, T, y, ids_out, w_out, ws, dev, s, resid);
+        default: return decode_impl<NVFP4_SCALE_UE8M0>(d, x, T, y, ids_out, w_out, ws, dev, s, resid);
+    }
 }
 
 }  // namespace nvfp4

@@ -1,0 +1,817 @@
+// One-launch decode of the MoE layer for a single token (T = 1).
+//
+// Sources (page title, section):
+//  - lynn-engine README, P45 note: the active-MoE path as one native call
+//    (hidden, expert ids, routing weights, gate/up and down weights -> out[H]);
+//    P28/P29 notes: gate/up + SiLU -> [top_k, I] intermediate, then down +
+//    routing-weighted sum; P46 note: a fused-atomic single kernel was slow and
+//    drifted, so the combine here has no atomics: every output row is owned by
+//    one block and summed in a fixed order (P48 note: non-atomic row ownership).
+//  - lynn-engine tutorials index, row 06: softmax over all experts -> top-k ->
+//    renormalise; sigmoid-gated shared expert.
+//  - Lynn Engine write-up, "CUDA Graph and scheduling": decode is launch-bound;
+//    here the whole layer is one launch.
+//
+// A persistent grid of one CTA per SM: 16 compute warps and one copy warp. Every
+// CTA owns contiguous ranges of each weight stream, so each stream is a handful of
+// large TMA bulk copies (cp.async.bulk, completing on mbarriers):
+//   router rows    [(E+1)c/G, (E+1)(c+1)/G)   (row E = the shared gate vector)
+//   shared pairs   [Is c/G, Is (c+1)/G)        (gate row, up row of the shared expert)
+//   routed pairs   [kI c/G, kI (c+1)/G)        (pair q = slot q / I, row q % I)
+//   output rows    [H c/G, H (c+1)/G)          (the down rows of every slot)
+//
+// Timeline of a CTA:
+//   before griddepcontrol.wait  the router rows, the shared pairs and the shared down
+//                               rows are requested (they depend on nothing the previous
+//                               kernel writes); under programmatic dependent launch they
+//                               stream in while that kernel finishes
+//   x                           staged raw (bf16, for the router) and as f16 times the
+//                               power of two 2^sx that puts max|x| in [2^14, 2^15)
+//   router rows                 bf16 dot products -> logit words (tag, value)
+//   shared pairs                hs words, computed while the other CTAs' logits arrive
+//   top-k                       every CTA gathers the E logits and takes the top-k itself
+//   routed copies               the CTA's routed pairs (4 chunks, one mbarrier each) and
+//                               its down rows of the k routed experts
+//   routed pairs                one warp per (gate, up) pair as its chunk lands -> h words
+//   h                           every CTA gathers the k*I + Is words, scales each slot by
+//                               a power of two into f16
+//   down                        one warp per output row: sum over the k + 1 slots in a
+//                               fixed order, one bf16 rounding
+//
+// Values that cross CTAs travel as tagged words: logits as 64-bit (tag << 32 | fp32 bits),
+// SwiGLU intermediates as 32-bit (16-bit tag << 16 | bf16 bits), read four per 16-byte load
+// (every CTA reads all k*I + Is of them, so the L2 request count is what this exchange
+// costs). A reader re-reads a word until it carries this launch's tag, so one L2 read both
+// waits and delivers the value; there is no separate grid barrier. The tag is floor(n / G)
+// + 1 where n counts CTA starts in the workspace header (one atomic per CTA). Every poll
+// is bounded in time; a poll that runs out records NVFP4_ERR_DEVICE_TIMEOUT, the CTA
+// drains its copies in flight and returns.
+//
+// Dot products: cvt.rn.f16x2.e2m1x2 expands two codes into an exact f16 pair and
+// fma.rn.f32.f16 multiplies each with its f16 activation and accumulates in fp32; each
+// 16-element partial is multiplied by its block scale (exact decode) in fp32. The
+// activation side is exact for x (bf16 -> f16 after a power-of-two scale); the SwiGLU
+// intermediate h is rounded once to bf16 when it is published (relative error 2^-9 per
+// element, the activation type and the prefill path's rounding) and then converted exactly
+// to f16 after a power-of-two scale per slot for the down pass.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kW = 16;                    // compute warps
+constexpr int kThr = (kW + 1) * 32;       // + the copy warp
+constexpr int kCopyWarp = kW;
+constexpr int kChunks = 4;                // routed-pair copy chunks (one mbarrier each)
+constexpr int kSlots = NVFP4_MAX_TOPK + 1;
+
+struct T1Params {
+    moe_layer_desc d;
+    const uint16_t* x;
+    uint16_t* y;
+    int32_t* ids_out;
+    float* w_out;
+    WsHeader* hdr;
+    unsigned long long* words;    // [E + 1] logits and gate, then [k*I + Is] h and hs
+    unsigned long long wait_limit;
+    const uint16_t* norm_w;       // nullable: x = bf16(RMSNorm_(1+w)(input)) first
+    float eps;
+    const uint16_t* resid;        // nullable: y = bf16(resid + layer)
+    // shared-memory layout (bytes), identical for every CTA
+    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_h16;
+    uint32_t sg_reg;      // bytes of one region of the shared-pair area (codes)
+    uint32_t sg_sreg;     // ... (scales)
+    uint32_t gu_reg;      // bytes of one region of the routed-pair area (codes)
+    uint32_t gu_sreg;     // ... (scales)
+    uint32_t dn_slot;     // bytes of one slot of the down area (codes, then scales)
+    uint32_t dn_sc;       // offset of the scales inside a down slot
+    unsigned long long mG64;   // ceil(2^64 / G)
+};
+
+__device__ __forceinline__ void st_word(unsigned long long* p, uint32_t tag, float v) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long* p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+// Read a word until it carries `tag` (bounded); false on timeout.
+__device__ __forceinline__ bool poll_word(const unsigned long long* p, uint32_t tag, unsigned long long limit,
+                                          float* out) {
+    unsigned long long w = ld_word(p);
+    if ((uint32_t)(w >> 32) != tag) {
+        const unsigned long long t0 = global_timer_ns();
+        do {
+            if (global_timer_ns() - t0 > limit) return false;
+            w = ld_word(p);
+        } while ((uint32_t)(w >> 32) != tag);
+    }
+    *out = __uint_as_float((uint32_t)w);
+    return true;
+}
+
+// h words: the low 16 bits of the launch tag (never 0) over the bf16 value, single-copy
+// atomic as one 32-bit store; readers load four at a time.
+__device__ __forceinline__ uint32_t tag16_of(uint32_t tag) { return tag % 65535u + 1u; }
+__device__ __forceinline__ void st_hword(uint32_t* p, uint32_t tag16, float v) {
+    const uint32_t w = (tag16 << 16) | (uint32_t)f32_to_bf16(v);
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(w) : "memory");
+}
+// eight words (32 bytes, 32-byte aligned) in one load
+__device__ __forceinline__ void ld_hwords8(const uint32_t* p, uint4& a, uint4& b) {
+    asm volatile("ld.relaxed.gpu.global.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void expand4(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
+}
+
+__device__ __forceinline__ float fma2h(uint32_t q2, uint32_t x2, float acc) {
+    asm("{\n .reg .f16 ql, qh, xl, xh;\n mov.b32 {ql, qh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+        " fma.rn.f32.f16 %0, ql, xl, %0;\n fma.rn.f32.f16 %0, qh, xh, %0;\n}"
+        : "+f"(acc) : "r"(q2), "r"(x2));
+    return acc;
+}
+
+__device__ __forceinline__ uint32_t to_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// k with m * 2^k in [2^14, 2^15) from the fp32 bits of m >= 0 (0 for m = 0), clamped so
+// that 2^k and 2^-k are normal.
+__device__ __forceinline__ int pow2_shift(uint32_t fbits) {
+    if (fbits == 0u) return 0;
+    const int e = (int)(fbits >> 23) - 127;
+    return min(126, max(-126, 14 - e));
+}
+__device__ __forceinline__ float exp2_int(int k) { return __int_as_float((k + 127) << 23); }
+
+template <int KIND>
+__device__ __forceinline__ void scales2(const uint8_t* srow, int s, float& s0, float& s1) {
+    if constexpr (KIND == NVFP4_SCALE_E4M3) {
+        const uint32_t b = *reinterpret_cast<const uint16_t*>(srow + 2 * s);
+        s0 = e4m3_to_f32(b & 0xFFu);
+        s1 = e4m3_to_f32(b >> 8);
+    } else {
+        const uint32_t h = *reinterpret_cast<const uint32_t*>(srow + 4 * s);
+        s0 = f16_bits_to_f32(static_cast<uint16_t>(h & 0xFFFFu));
+        s1 = f16_bits_to_f32(static_cast<uint16_t>(h >> 16));
+    }
+}
+
+// One 16-byte segment (32 codes, two scale blocks) against 32 f16 activations stored
+// segment-interleaved (unit c of segment s at c * nseg + s).
+template <int KIND>
+__device__ __forceinline__ float seg_dot(const uint4 w, float s0, float s1, const uint4* xv, int nseg, int s) {
+    uint32_t a[4], b[4], c[4], d[4];
+    expand4(w.x, a);
+    expand4(w.y, b);
+    expand4(w.z, c);
+    expand4(w.w, d);
+    const uint4 u0 = xv[s], u1 = xv[nseg + s], u2 = xv[2 * nseg + s], u3 = xv[3 * nseg + s];
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    p0 = fma2h(a[0], u0.x, p0); p1 = fma2h(a[1], u0.y, p1); p0 = fma2h(a[2], u0.z, p0); p1 = fma2h(a[3], u0.w, p1);
+    p0 = fma2h(b[0], u1.x, p0); p1 = fma2h(b[1], u1.y, p1); p0 = fma2h(b[2], u1.z, p0); p1 = fma2h(b[3], u1.w, p1);
+    p2 = fma2h(c[0], u2.x, p2); p3 = fma2h(c[1], u2.y, p3); p2 = fma2h(c[2], u2.z, p2); p3 = fma2h(c[3], u2.w, p3);
+    p2 = fma2h(d[0], u3.x, p2); p3 = fma2h(d[1], u3.y, p3); p2 = fma2h(d[2], u3.z, p2); p3 = fma2h(d[3], u3.w, p3);
+    return fmaf(s0, p0 + p1, s1 * (p2 + p3));
+}
+
+// (gate . x, up . x) of one pair whose rows sit in shared memory; lanes over segments.
+// Lane 0 ends with the gate sum, lane 16 with the up sum.
+template <int KIND>
+__device__ __noinline__ float pair_dot(const uint8_t* g, const uint8_t* u, const uint8_t* gs, const uint8_t* us,
+                                       const uint4* x16, int nseg, int lane) {
+    float ga = 0.f, ua = 0.f;
+#pragma unroll 2
+    for (int s = lane; s < nseg; s += 32) {
+        float g0, g1, u0, u1;
+        scales2<KIND>(gs, s, g0, g1);
+        scales2<KIND>(us, s, u0, u1);
+        ga += seg_dot<KIND>(reinterpret_cast<const uint4*>(g)[s], g0, g1, x16, nseg, s);
+        ua += seg_dot<KIND>(reinterpret_cast<const uint4*>(u)[s], u0, u1, x16, nseg, s);
+    }
+    const bool lo = lane < 16;
+    float m = lo ? ga : ua;
+    m += __shfl_xor_sync(0xffffffffu, lo ? ua : ga, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    return m;
+}
+
+__device__ __forceinline__ float bf16_dot8(const uint4 w, const uint4 v, float acc) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t xx[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc = fmaf(bf16lo(ww[q]), bf16lo(xx[q]), acc);
+        acc = fmaf(bf16hi(ww[q]), bf16hi(xx[q]), acc);
+    }
+    return acc;
+}
+
+// float -> unsigned key with the same order
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ uint32_t copy_range(uint8_t* dst, const uint8_t* src, uint32_t bytes, uint64_t* bar) {
+    if (bytes) bulk_g2s(dst, src, bytes, bar);
+    return bytes;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ uint64_t mbA, mbS, mbB[kChunks];
+    __shared__ int s_ids[NVFP4_MAX_TOPK];
+    __shared__ float s_coef[kSlots];                       // down coefficient of each slot
+    __shared__ float s_tsg[kSlots], s_tsu[kSlots];
+    __shared__ uint32_t s_hmax[kSlots];
+    __shared__ uint32_t s_xmax, s_tag;
+    __shared__ int s_fail;
+    __shared__ float s_ss[kThr / 32];
+    __shared__ float s_tg[NVFP4_MAX_EXPERTS * 2], s_td[NVFP4_MAX_EXPERTS];   // every expert's tensor scales
+
+    const moe_layer_desc& d = P.d;
+    const int H = d.H, E = d.E, k = d.k, I = d.I, Is = d.Is;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int sb = KIND == NVFP4_SCALE_E4M3 ? 1 : 2;
+    const uint32_t rowH = H / 2, srowH = H / 16 * sb;     // bytes of a code / scale row of K = H
+    const int nsegH = H >> 5, nunitH = H >> 3;
+    const int nR0 = (int)((long long)(E + 1) * c / G), nR1 = (int)((long long)(E + 1) * (c + 1) / G);
+    const int s0 = (int)((long long)Is * c / G), s1 = (int)((long long)Is * (c + 1) / G);
+    const int q0 = (int)((long long)k * I * c / G), q1 = (int)((long long)k * I * (c + 1) / G);
+    const int n0 = (int)((long long)H * c / G), n1 = (int)((long long)H * (c + 1) / G);
+    const int nR = nR1 - nR0, nS = s1 - s0, nq = q1 - q0, nN = n1 - n0;
+    const int total = k * I;
+    // every word is written to kWordReplicas copies and CTA c reads copy c % kWordReplicas:
+    // the exchanged lines are read by every CTA, and one L2 line read by all 152 CTAs
+    // serialises their requests, so each copy is read by only ~G / kWordReplicas of them
+    const size_t lg_stride = t1_logit_stride(d), h_stride = t1_h_stride(d);
+    const int rep = c % kWordReplicas;
+    unsigned long long* w_lg_all = P.words;
+    uint32_t* w_h_all = reinterpret_cast<uint32_t*>(P.words + kWordReplicas * lg_stride);
+    const unsigned long long* w_lg = w_lg_all + rep * lg_stride;     // this CTA's copy
+    const uint32_t* w_h = w_h_all + rep * h_stride;
+
+    uint16_t* xb = reinterpret_cast<uint16_t*>(sm + P.o_xb);
+    uint4* x16 = reinterpret_cast<uint4*>(sm + P.o_x16);
+    float* lg = reinterpret_cast<float*>(sm + P.o_lg);
+    uint8_t* RT = sm + P.o_rt;
+    uint8_t* SG = sm + P.o_sg;                // regions: gate codes, up codes, gate scales, up scales
+    uint8_t* GU = sm + P.o_gu;                // same four regions for the routed pairs
+    uint8_t* DN = sm + P.o_dn;                // slot j: codes [nN][I/2], then scales [nN][I/16*sb]
+    uint4* h16 = reinterpret_cast<uint4*>(sm + P.o_h16);
+
+    // ------------------------------------------------------------------ prologue
+    if (tid == 0) {
+        mbar_init(&mbA, 1);
+        mbar_init(&mbS, 1);
+        for (int i = 0; i < kChunks; ++i) mbar_init(&mbB[i], 1);
+        fence_mbar_init();
+        s_fail = 0;
+        s_xmax = 0u;
+        for (int j = 0; j < kSlots; ++j) s_hmax[j] = 0u;
+    }
+    __syncthreads();
+    const uint8_t* sh_gu = d.sh_gu_packed;
+    const uint8_t* sh_gus = static_cast<const uint8_t*>(d.sh_gu_scales);
+    const uint32_t rowS = Is / 2, srowS = Is / 16 * sb;
+    if (warp == kCopyWarp) {
+        // weight-only copies: router rows, shared pairs, shared down rows
+        if (lane == 0) {
+            const uint32_t a = (uint32_t)(min(nR1, E) - min(nR0, E)) * 2u * H + (nR1 > E ? 2u * H : 0u) +
+                               (uint32_t)nS * 2u * (rowH + srowH);
+            mbar_arrive_expect_tx(&mbA, a);
+            mbar_arrive_expect_tx(&mbS, Is > 0 ? (uint32_t)nN * (rowS + srowS) : 0u);
+        }
+        __syncwarp();
+        const int rE = min(nR1, E) - min(nR0, E);   // router rows of this CTA below E
+        if (lane == 0 && rE > 0)
+            copy_range(RT, reinterpret_cast<const uint8_t*>(d.router_w + (size_t)nR0 * H), (uint32_t)rE * 2u * H, &mbA);
+        if (lane == 1 && nR1 > E)
+            copy_range(RT + (size_t)rE * 2 * H, reinterpret_cast<const uint8_t*>(d.sh_gate_w), 2u * H, &mbA);
+        if (nS > 0) {
+            if (lane == 2) copy_range(SG, sh_gu + (size_t)s0 * rowH, (uint32_t)nS * rowH, &mbA);
+            if (lane == 3) copy_range(SG + P.sg_reg, sh_gu + (size_t)(Is + s0) * rowH, (uint32_t)nS * rowH, &mbA);
+            if (lane == 4) copy_range(SG + 2 * P.sg_reg, sh_gus + (size_t)s0 * srowH, (uint32_t)nS * srowH, &mbA);
+            if (lane == 5)
+                copy_range(SG + 2 * P.sg_reg + P.sg_sreg, sh_gus + (size_t)(Is + s0) * srowH, (uint32_t)nS * srowH, &mbA);
+        }
+        if (Is > 0) {
+            uint8_t* dsl = DN + (size_t)k * P.dn_slot;
+            if (lane == 6) copy_range(dsl, d.sh_dn_packed + (size_t)n0 * rowS, (uint32_t)nN * rowS, &mbS);
+            if (lane == 7)
+                copy_range(dsl + P.dn_sc, static_cast<const uint8_t*>(d.sh_dn_scales) + (size_t)n0 * srowS,
+                           (uint32_t)nN * srowS, &mbS);
+        }
+    }
+
+    // every expert's tensor scales (read after the top-k): requested now into registers, written
+    // to shared memory after the x staging, so no thread waits for them
+    float tsv[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int i = tid + u * kThr;
+        if (i < 2 * E) tsv[u] = __ldg(d.gu_tscale + i);
+        else if (i < 3 * E) tsv[u] = __ldg(d.dn_tscale + (i - 2 * E));
+    }
+    float sh_tsg = 0.f, sh_tsu = 0.f, sh_tsd = 0.f;
+    if (Is > 0) {
+        sh_tsg = __ldg(d.sh_gu_tscale);
+        sh_tsu = __ldg(d.sh_gu_tscale + 1);
+        sh_tsd = __ldg(d.sh_dn_tscale);
+    }
+
+    // everything below may read what the previous kernel on the stream wrote
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (tid == 0) {
+        unsigned long long n;
+        asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n) : "l"(&P.hdr->barrier) : "memory");
+        unsigned long long q = __umul64hi(n, P.mG64);    // n / G, corrected below
+        if ((q + 1) * (unsigned long long)G <= n) ++q;
+        if (q * (unsigned long long)G > n) --q;
+        s_tag = (uint32_t)q + 1u;
+    }
+    // x: raw bf16 for the router, and max |x| for the f16 copy
+    uint4 xv = make_uint4(0, 0, 0, 0);
+    if (tid < nunitH) xv = reinterpret_cast<const uint4*>(P.x)[tid];
+    if (P.norm_w) {
+        // pre-MoE RMSNorm (1 + w) x / sqrt(mean(x^2) + eps): squares summed per thread, per
+        // warp by shuffles, then over the warps in a fixed order; rounded once to bf16
+        float ss = 0.f;
+        {
+            const uint32_t ww[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ss = fmaf(bf16lo(ww[q]), bf16lo(ww[q]), ss);
+                ss = fmaf(bf16hi(ww[q]), bf16hi(ww[q]), ss);
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s_ss[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < kThr / 32; ++i) tot += s_ss[i];
+        const float r = 1.0f / sqrtf(tot / (float)H + P.eps);
+        if (tid < nunitH) {
+            const uint4 wv = reinterpret_cast<const uint4*>(P.norm_w)[tid];
+            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w}, nw[4] = {wv.x, wv.y, wv.z, wv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = bf16lo(xx[q]) * r * (1.0f + bf16lo(nw[q]));
+                const float hi = bf16hi(xx[q]) * r * (1.0f + bf16hi(nw[q]));
+                o[q] = (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+            }
+            xv = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (tid < nunitH) {
+        reinterpret_cast<uint4*>(xb)[tid] = xv;
+        const uint32_t ww[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t m = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = max(m, max(ww[q] & 0x7FFFu, (ww[q] >> 16) & 0x7FFFu));
+        m = __reduce_max_sync(__activemask(), m);
+        if (lane == 0) atomicMax(&s_xmax, m << 16);     // as fp32 bits
+    }
+    __syncthreads();
+    const uint32_t tag = s_tag, tag16 = tag16_of(tag);
+    const int sx = pow2_shift(s_xmax);
+    if (tid < nunitH) {
+        const float sc = exp2_int(sx);
+        uint4 o;
+        o.x = to_f16x2(bf16lo(xv.x) * sc, bf16hi(xv.x) * sc);
+        o.y = to_f16x2(bf16lo(xv.y) * sc, bf16hi(xv.y) * sc);
+        o.z = to_f16x2(bf16lo(xv.z) * sc, bf16hi(xv.z) * sc);
+        o.w = to_f16x2(bf16lo(xv.w) * sc, bf16hi(xv.w) * sc);
+        x16[(tid & 3) * nsegH + (tid >> 2)] = o;
+    }
+    __syncthreads();
+    const float inv_x = exp2_int(-sx);
+
+    bool ok = true;
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const int i = tid + u * kThr;
+        if (i < 2 * E) s_tg[i] = tsv[u];
+        else if (i < 3 * E) s_td[i - 2 * E] = tsv[u];
+    }
+    if (warp < kW) {
+        // router rows (warps 0 .. nR-1) and shared pairs (the other warps)
+        ok = mbar_wait_bounded(&mbA, 0, kDefaultWaitLimit);
+        if (ok) {
+            for (int t = warp; t < nR + nS; t += kW) {
+                if (t < nR) {
+                    const uint4* wr = reinterpret_cast<const uint4*>(RT + (size_t)t * 2 * H);
+                    const uint4* xr = reinterpret_cast<const uint4*>(xb);
+                    float acc = 0.f;
+#pragma unroll 4
+                    for (int ch = lane; ch < nunitH; ch += 32) acc = bf16_dot8(wr[ch], xr[ch], acc);
+                    acc = warp_sum(acc);
+                    if (lane < kWordReplicas) st_word(w_lg_all + lane * lg_stride + nR0 + t, tag, acc);
+                } else {
+                    const int j = t - nR;
+                    const float m = pair_dot<KIND>(SG + (size_t)j * rowH, SG + P.sg_reg + (size_t)j * rowH,
+                                                   SG + 2 * P.sg_reg + (size_t)j * srowH,
+                                                   SG + 2 * P.sg_reg + P.sg_sreg + (size_t)j * srowH, x16, nsegH, lane);
+                    const float gsum = __shfl_sync(0xffffffffu, m, 0), usum = __shfl_sync(0xffffffffu, m, 16);
+                    if (lane < kWordReplicas) {
+                        const float hv = silu_f32(gsum * inv_x * sh_tsg) * (usum * inv_x * sh_tsu);
+                        st_hword(w_h_all + lane * h_stride + total + s0 + j, tag16, hv);
+                    }
+                }
+            }
+        }
+        asm volatile("griddepcontrol.launch_dependents;");
+        // gather the E logits and the gate pre-activation
+        if (ok) {
+            for (int e = tid; e <= E; e += kW * 32) {
+                float v;
+                if (!poll_word(w_lg + e, tag, P.wait_limit, &v)) { ok = false; break; }
+                lg[e] = v;
+            }
+        }
+    }
+    if (warp == kCopyWarp) asm volatile("griddepcontrol.launch_dependents;");
+    if (!ok) s_fail = 1;
+    __syncthreads();
+    if (s_fail) {
+        if (tid == 0) record_status(P.hdr, NVFP4_ERR_DEVICE_TIMEOUT);
+        if (tid == 0) {
+            mbar_wait_bounded(&mbA, 0, kDefaultWaitLimit);
+            mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ top-k
+    if (warp == 0) {
+        uint32_t key[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) key[i] = lane + 32 * i < E ? order_key(lg[lane + 32 * i]) : 0u;
+        int my_id = -1;
+        float ex = 0.f, vmax = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            uint32_t best = key[0];
+            int bi = 0;
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                if (key[i] > best) { best = key[i]; bi = i; }   // strict: the lower id wins ties
+            const uint32_t wb = __reduce_max_sync(0xffffffffu, best);
+            const uint32_t e = __reduce_min_sync(0xffffffffu, best == wb ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+            if ((int)(e & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i == bi) key[i] = 0u;
+            }
+            const float v = key_value(wb);
+            if (j == 0) vmax = v;
+            if (lane == j) { my_id = (int)e; ex = __expf(v - vmax); }
+        }
+        const float sum = warp_sum(lane < k ? ex : 0.f);
+        if (lane < k) {
+            const float wj = __fdividef(ex, sum);
+            s_ids[lane] = my_id;
+            s_coef[lane] = wj;
+            s_tsg[lane] = s_tg[2 * my_id];
+            s_tsu[lane] = s_tg[2 * my_id + 1];
+            if (c == 0) {
+                if (P.ids_out) P.ids_out[lane] = my_id;
+                if (P.w_out) P.w_out[lane] = wj;
+            }
+        }
+        if (lane == 0 && Is > 0) s_coef[k] = sigmoid_f32(lg[E]) * sh_tsd;
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------------ routed copies
+    const uint8_t* gu_p = d.gu_packed;
+    const uint8_t* gu_s = static_cast<const uint8_t*>(d.gu_scales);
+    const uint32_t rowI = I / 2, srowI = I / 16 * sb;
+    if (warp == kCopyWarp) {
+        // chunk ch holds local pairs [nq ch / 4, nq (ch+1) / 4): at most two slots ("pieces");
+        // lane = 8 ch + 4 piece + part issues one contiguous copy (gate codes, up codes,
+        // gate scales, up scales) of the piece's pairs
+        if (lane < kChunks) {
+            const int a = nq * lane / kChunks, b = nq * (lane + 1) / kChunks;
+            mbar_arrive_expect_tx(&mbB[lane], (uint32_t)(b - a) * 2u * (rowH + srowH));
+        }
+        __syncwarp();
+        {
+            const int ch = lane >> 3, piece = (lane >> 2) & 1, part = lane & 3;
+            const int qa = q0 + nq * ch / kChunks, qb = q0 + nq * (ch + 1) / kChunks;
+            if (qb > qa) {
+                const int ja = qa / I;
+                const int qs = piece == 0 ? qa : (ja + 1) * I;
+                const int qe = piece == 0 ? min(qb, (ja + 1) * I) : qb;
+                if (qe > qs) {
+                    const int j = qs / I, i0 = qs - j * I, r0 = qs - q0, nr = qe - qs;
+                    const size_t grow = (size_t)s_ids[j] * 2 * I + i0 + (part & 1) * I;   // first gate / up row
+                    if (part < 2)
+                        copy_range(GU + (part ? P.gu_reg : 0u) + (size_t)r0 * rowH, gu_p + grow * rowH,
+                                   (uint32_t)nr * rowH, &mbB[ch]);
+                    else
+                        copy_range(GU + 2 * P.gu_reg + (part == 3 ? P.gu_sreg : 0u) + (size_t)r0 * srowH,
+                                   gu_s + grow * srowH, (uint32_t)nr * srowH, &mbB[ch]);
+                }
+            }
+        }
+    } else {
+        // the k routed experts' down rows of this CTA's output rows, 16 bytes per cp.async from
+        // every compute thread: they are read last, and the SM's TMA unit handles one bulk copy
+        // at a time, so these small pieces stay off its queue
+        {
+            const int pr = (int)(rowI >> 4), ps = (int)(srowI >> 4);   // 16-byte pieces per row
+            const int per_slot = nN * (pr + ps);
+            for (int i = tid; i < k * per_slot; i += kW * 32) {
+                const int j = i / per_slot, r = i - j * per_slot;
+                const size_t rb = (size_t)s_ids[j] * H + n0;
+                uint8_t* dsl = DN + (size_t)j * P.dn_slot;
+                if (r < nN * pr) {
+                    cp_async16(dsl + 16 * (size_t)r, d.dn_packed + rb * rowI + 16 * (size_t)r);
+                } else {
+                    const int q = r - nN * pr;
+                    cp_async16(dsl + P.dn_sc + 16 * (size_t)q,
+                               static_cast<const uint8_t*>(d.dn_scales) + rb * srowI + 16 * (size_t)q);
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        // ---------------------------------------------------------------- routed pairs
+        for (int r = warp; r < nq; r += kW) {
+            int ch = 0;
+            while (ch + 1 < kChunks && r >= nq * (ch + 1) / kChunks) ++ch;
+            if (ok && !mbar_wait_bounded(&mbB[ch], 0, kDefaultWaitLimit)) ok = false;
+            if (!ok) break;
+            const float m = pair_dot<KIND>(GU + (size_t)r * rowH, GU + P.gu_reg + (size_t)r * rowH,
+                                           GU + 2 * P.gu_reg + (size_t)r * srowH,
+                                           GU + 2 * P.gu_reg + P.gu_sreg + (size_t)r * srowH, x16, nsegH, lane);
+            const float gsum = __shfl_sync(0xffffffffu, m, 0), usum = __shfl_sync(0xffffffffu, m, 16);
+            if (lane < kWordReplicas) {
+                const int q = q0 + r, j = q / I;
+                const float hv = silu_f32(gsum * inv_x * s_tsg[j]) * (usum * inv_x * s_tsu[j]);
+                st_hword(w_h_all + lane * h_stride + q, tag16, hv);
+            }
+        }
+        // ---------------------------------------------------------------- gather h
+        // every thread reads 8-word units of the k*I + Is words (one 32-byte load each, all in
+        // flight), re-reads the units with an untagged word until all carry this launch's
+        // tag (bounded), then stages them for the down pass
+        constexpr int kMaxU = 2;    // units per thread: (k*I + Is) <= 16 * 512
+        const int nh = total + Is, nu = nh >> 3;
+        uint4 wa[kMaxU], wb[kMaxU];
+#pragma unroll
+        for (int u = 0; u < kMaxU; ++u) {
+            const int i = tid + u * kW * 32;
+            wa[u] = wb[u] = make_uint4(0, 0, 0, 0);
+            if (i < nu) ld_hwords8(w_h + 8 * i, wa[u], wb[u]);
+        }
+        auto ready4 = [&](const uint4 w) {
+            return (w.x >> 16) == tag16 && (w.y >> 16) == tag16 && (w.z >> 16) == tag16 && (w.w >> 16) == tag16;
+        };
+        {
+            unsigned long long t0 = 0;
+            for (int round = 0; ok; ++round) {
+                bool pending = false;
+#pragma unroll
+                for (int u = 0; u < kMaxU; ++u)
+                    if (tid + u * kW * 32 < nu && !(ready4(wa[u]) && ready4(wb[u]))) pending = true;
+                if (!pending) break;
+                if (round == 0) t0 = global_timer_ns();
+                else if (global_timer_ns() - t0 > P.wait_limit) { ok = false; break; }
+#pragma unroll
+                for (int u = 0; u < kMaxU; ++u) {
+                    const int i = tid + u * kW * 32;
+                    if (i < nu && !(ready4(wa[u]) && ready4(wb[u]))) ld_hwords8(w_h + 8 * i, wa[u], wb[u]);
+                }
+            }
+        }
+        // per-slot maxima (a warp's 256 consecutive words lie in one slot: I % 256 == 0)
+#pragma unroll
+        for (int u = 0; u < kMaxU; ++u) {
+            const int base = 8 * (warp * 32 + u * kW * 32);   // first word of this warp's 256
+            if (base < nh) {
+                const uint4 a = wa[u], b = wb[u];
+                uint32_t m = max(max(a.x & 0x7FFFu, a.y & 0x7FFFu), max(a.z & 0x7FFFu, a.w & 0x7FFFu));
+                m = max(m, max(max(b.x & 0x7FFFu, b.y & 0x7FFFu), max(b.z & 0x7FFFu, b.w & 0x7FFFu)));
+                m = __reduce_max_sync(0xffffffffu, m);
+                if (lane == 0) atomicMax(&s_hmax[base < total ? base / I : k], m << 16);
+            }
+        }
+        named_sync(1, kW * 32);
+        // slot j's values as f16 times 2^sh_j, segment-interleaved per slot; a unit's eight
+        // consecutive elements are one 16-byte store
+#pragma unroll
+        for (int u = 0; u < kMaxU; ++u) {
+            const int i = tid + u * kW * 32;
+            if (i < nu && ok) {
+                const int e0 = 8 * i;
+                const int j = e0 < total ? e0 / I : k;
+                const int e = e0 < total ? e0 - j * I : e0 - total;
+                const int K = j < k ? I : Is;
+                const float sc = exp2_int(pow2_shift(s_hmax[j]));
+                const uint4 a = wa[u], b = wb[u];
+                const uint4 o = make_uint4(to_f16x2(bf16lo(a.x) * sc, bf16lo(a.y) * sc),
+                                           to_f16x2(bf16lo(a.z) * sc, bf16lo(a.w) * sc),
+                                           to_f16x2(bf16lo(b.x) * sc, bf16lo(b.y) * sc),
+                                           to_f16x2(bf16lo(b.z) * sc, bf16lo(b.w) * sc));
+                const int u8 = e >> 3, nseg = K >> 5;
+                h16[(size_t)j * (I >> 3) + (u8 & 3) * nseg + (u8 >> 2)] = o;
+            }
+        }
+    }
+    if (warp < kW) asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's down-row pieces
+    if (!ok) s_fail = 1;
+    __syncthreads();
+    if (s_fail || !mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit)) {
+        if (tid == 0) {
+            record_status(P.hdr, NVFP4_ERR_DEVICE_TIMEOUT);
+            for (int i = 0; i < kChunks; ++i) mbar_wait_bounded(&mbB[i], 0, kDefaultWaitLimit);
+            mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit);
+        }
+        return;
+    }
+    // chunks that no warp waited for (a CTA with fewer pairs than warps waits for all)
+    if (tid == 0)
+        for (int i = 0; i < kChunks; ++i) mbar_wait_bounded(&mbB[i], 0, kDefaultWaitLimit);
+
+    // ------------------------------------------------------------------ down
+    if (warp < kW) {
+        const int nsegI = I >> 5, nsegS = Is >> 5;
+        const int work = k * nsegI + nsegS;
+        float coef[kSlots];
+#pragma unroll
+        for (int j = 0; j < kSlots; ++j) {
+            coef[j] = 0.f;
+            if (j < k) coef[j] = s_coef[j] * s_td[s_ids[j]] * exp2_int(-pow2_shift(s_hmax[j]));
+            else if (j == k && Is > 0) coef[j] = s_coef[k] * exp2_int(-pow2_shift(s_hmax[k]));
+        }
+        for (int nl = warp; nl < nN; nl += kW) {
+            // lane l sums the weighted segments l, l + 32, ... of the (slot, segment) list in
+            // that order, then the warp is reduced once: a fixed order, no atomics
+            float acc = 0.f;
+            int j = 0, s = lane;               // (slot, segment) of item p = lane + 32 m
+            while (j < k && s >= nsegI) { s -= nsegI; ++j; }
+#pragma unroll 1
+            for (int p = lane; p < work; p += 32) {
+                if (j == k && s >= nsegS) break;
+                const int K = j < k ? I : Is;
+                const uint32_t rb = K / 2, srb = K / 16 * sb;
+                const uint8_t* dsl = DN + (size_t)j * P.dn_slot;
+                float sa, sb2;
+                scales2<KIND>(dsl + P.dn_sc + (size_t)nl * srb, s, sa, sb2);
+                const float v = seg_dot<KIND>(reinterpret_cast<const uint4*>(dsl + (size_t)nl * rb)[s], sa, sb2,
+                                              h16 + (size_t)j * (I >> 3), K >> 5, s);
+                float cj = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < kSlots; ++jj)
+                    if (jj == j) cj = coef[jj];
+                acc = fmaf(cj, v, acc);
+                s += 32;
+                while (j < k && s >= nsegI) { s -= nsegI; ++j; }
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) {
+                if (P.resid) acc += bf16_to_f32(P.resid[n0 + nl]);   // residual stream, before the rounding
+                P.y[n0 + nl] = f32_to_bf16(acc);
+            }
+        }
+    }
+}
+
+struct T1Layout {
+    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_h16, total;
+    uint32_t sg_reg, sg_sreg, gu_reg, gu_sreg, dn_slot, dn_sc;
+};
+
+uint32_t a16(size_t v) { return (uint32_t)((v + 15) & ~size_t(15)); }
+
+T1Layout t1_layout(const moe_layer_desc& d, int G) {
+    const size_t sb = d.kind == NVFP4_SCALE_E4M3 ? 1 : 2;
+    const size_t H = d.H, I = d.I, Is = d.Is, k = d.k, E = d.E;
+    const size_t nR = (E + 1 + G - 1) / G + 1, nS = (Is + G - 1) / G + 1;
+    const size_t nq = (k * I + G - 1) / G + 1, nN = (H + G - 1) / G + 1;
+    const size_t Im = I > Is ? I : Is;
+    T1Layout L;
+    L.sg_reg = a16(nS * (H / 2));
+    L.sg_sreg = a16(nS * (H / 16 * sb));
+    L.gu_reg = a16(nq * (H / 2));
+    L.gu_sreg = a16(nq * (H / 16 * sb));
+    L.dn_sc = a16(nN * (Im / 2));
+    L.dn_slot = L.dn_sc + a16(nN * (Im / 16 * sb));
+    size_t off = 0;
+    L.o_xb = (uint32_t)off; off += a16(H * 2);
+    L.o_x16 = (uint32_t)off; off += a16(H * 2);
+    L.o_lg = (uint32_t)off; off += a16((E + 1) * 4);
+    L.o_rt = (uint32_t)off; off += a16(nR * H * 2);
+    L.o_sg = (uint32_t)off; off += 2 * (size_t)L.sg_reg + 2 * (size_t)L.sg_sreg;
+    L.o_gu = (uint32_t)off; off += 2 * (size_t)L.gu_reg + 2 * (size_t)L.gu_sreg;
+    L.o_dn = (uint32_t)off; off += (size_t)L.dn_slot * (k + 1);
+    L.o_h16 = (uint32_t)off; off += a16((k + 1) * Im * 2);
+    L.total = (uint32_t)off;
+    return L;
+}
+
+}  // namespace
+
+bool fused_decode_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev) {
+    const bool dims = d.H % 256 == 0 && d.I % 256 == 0 && (d.Is == 0 || d.Is % 256 == 0) && d.H <= 4096 &&
+                      d.I <= 4096 && d.Is <= 4096;
+    // h words per thread: (k*I + Is) <= 16 * 512; output rows per CTA fit the slot area
+    const bool kinds = d.kind == NVFP4_SCALE_E4M3 || d.kind == NVFP4_SCALE_FP16;
+    return T == 1 && dims && kinds && d.k * d.I + d.Is <= 16 * kW * 32 && (d.Is == 0 || d.Is <= d.I) &&
+           t1_layout(d, dev.num_sms).total <= dev.smem_optin;
+}
+
+cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, uint16_t* y,
+                                    int32_t* ids_out, float* w_out, const LayerWs& ws,
+                                    const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s,
+                                    const uint16_t* norm_w, float eps, const uint16_t* resid) {
+    const int G = dev.num_sms;
+    const T1Layout L = t1_layout(d, G);
+    if (L.total > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    T1Params P;
+    P.d = d;
+    P.x = x;
+    P.y = y;
+    P.ids_out = ids_out;
+    P.w_out = w_out;
+    P.hdr = ws.hdr;
+    P.words = ws.words;
+    P.wait_limit = wait_limit;
+    P.norm_w = norm_w;
+    P.eps = eps;
+    P.resid = resid;
+    P.o_xb = L.o_xb;
+    P.o_x16 = L.o_x16;
+    P.o_lg = L.o_lg;
+    P.o_rt = L.o_rt;
+    P.o_sg = L.o_sg;
+    P.o_gu = L.o_gu;
+    P.o_dn = L.o_dn;
+    P.o_h16 = L.o_h16;
+    P.sg_reg = L.sg_reg;
+    P.sg_sreg = L.sg_sreg;
+    P.gu_reg = L.gu_reg;
+    P.gu_sreg = L.gu_sreg;
+    P.dn_slot = L.dn_slot;
+    P.dn_sc = L.dn_sc;
+    P.mG64 = ~0ull / (unsigned long long)G + 1ull;
+    auto kern = d.kind == NVFP4_SCALE_E4M3 ? moe_decode_t1_kernel<NVFP4_SCALE_E4M3>
+                                           : moe_decode_t1_kernel<NVFP4_SCALE_FP16>;
+    // raise the dynamic shared-memory limit once per (device, kind, size)
+    static std::atomic<uint32_t> set_bytes[2][64];
+    const int ki = d.kind == NVFP4_SCALE_E4M3 ? 0 : 1;
+    const int dv = dev.device < 64 ? dev.device : 63;
+    if (set_bytes[ki][dv].load(std::memory_order_relaxed) < L.total) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+        if (err != cudaSuccess) return err;
+        set_bytes[ki][dv].store(L.total, std::memory_order_relaxed);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kThr);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+}  // namespace nvfp4

@@ -343,7 +343,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // 6. combine: y[t] = sum over the token's k routed rows, then the shared row, in
 //    that fixed order; one thread per 4 output features.
 __global__ void combine_kernel(const float* __restrict__ Y, int T, int H, int k, int n_slots,
-                               uint16_t* __restrict__ y) {
+                               const uint16_t* __restrict__ resid, uint16_t* __restrict__ y) {
     const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int q = H / 4;
     if (g >= (size_t)T * q) return;
@@ -353,6 +353,10 @@ __global__ void combine_kernel(const float* __restrict__ Y, int T, int H, int k,
     for (int j = 0; j < n_slots; ++j) {
         const float4 v = __ldcs(reinterpret_cast<const float4*>(src + (size_t)j * H));
         a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+    }
+    if (resid) {   // the residual stream, added before the one rounding
+        const uint2 r = *reinterpret_cast<const uint2*>(resid + (size_t)t * H + c);
+        a.x += bf16lo(r.x); a.y += bf16hi(r.x); a.z += bf16lo(r.y); a.w += bf16hi(r.y);
     }
     uint2 o;
     o.x = pack_bf16x2(a.x, a.y);
@@ -426,7 +430,7 @@ int prefill_launch_count(const moe_layer_desc& d, int T) {
 
 cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T, uint16_t* y,
                                int32_t* ids_out, float* w_out, const PrefillWs& ws, uint64_t wait_limit,
-                               cudaStream_t s) {
+                               cudaStream_t s, const uint16_t* resid) {
     const int E = d.E, k = d.k, H = d.H;
     const int total = T * k;
     int32_t* ids = ids_out ? ids_out : ws.ids;
@@ -483,7 +487,7 @@ cudaError_t launch_moe_prefill(const moe_layer_desc& d, const uint16_t* x, int T
     // 6. combine
     {
         const size_t n = (size_t)T * (H / 4);
-        combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.Y, T, H, k, k + (d.Is > 0 ? 1 : 0), y);
+        combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.Y, T, H, k, k + (d.Is > 0 ? 1 : 0), resid, y);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -81,10 +81,13 @@ __global__ void pack_quant_kernel(const float* __restrict__ w, size_t nblocks,
         const uint32_t e = e4m3_rne_satfinite(__fdiv_rn(r, s_t));
         static_cast<uint8_t*>(scales)[b] = static_cast<uint8_t>(e);
         dec = __fmul_rn(e4m3_to_f32(e), s_t);
-    } else {
+    } else if (KIND == NVFP4_SCALE_FP16) {
         const uint32_t e = f16_rne_satfinite(r);
         static_cast<uint16_t*>(scales)[b] = static_cast<uint16_t>(e);
         dec = __fmul_rn(f16_bits_to_f32(static_cast<uint16_t>(e)), s_t);
+    } else {   // FP32: the block scale itself
+        static_cast<float*>(scales)[b] = r;
+        dec = r;
     }
     uint32_t out[2] = {0u, 0u};
     if (dec > 0.0f) {
@@ -107,6 +110,48 @@ __global__ void pack_quant_kernel(const float* __restrict__ w, size_t nblocks,
     __threadfence();
 }
 
+// UE8M0: one thread per 32-element block; the scale is 2^(floor(log2 amax_b) - 2) (the OCP MX
+// rule: E2M1's largest power of two is 2^2), clamped to E8M0's range, 2^0 for a zero block;
+// the tensor scale is 1.
+__global__ void pack_quant_ue8m0_kernel(const float* __restrict__ w, size_t nblocks, uint8_t* __restrict__ packed,
+                                        uint8_t* __restrict__ scales, float* __restrict__ tensor_scale) {
+    const size_t b = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (b == 0) {
+        *tensor_scale = 1.0f;
+        __threadfence();
+    }
+    if (b >= nblocks) return;
+    const float4* src = reinterpret_cast<const float4*>(w + b * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = __ldg(src + i);
+        v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    }
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax_b = fmaxf(amax_b, fabsf(v[i]));
+    int ex = 0;
+    if (amax_b > 0.0f) {
+        const int be = (int)((__float_as_uint(amax_b) >> 23) & 0xFFu);   // 0 for subnormal amax
+        ex = be == 0 ? -127 : max(-127, min(127, be - 127 - 2));
+    }
+    scales[b] = static_cast<uint8_t>(ex + 127);
+    const float dec = ldexpf(1.0f, ex);
+    uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float lo = v[2 * j], hi = v[2 * j + 1];
+        uint32_t byte = e2m1_rne_satfinite(fabsf(__fdiv_rn(lo, dec))) |
+                        (e2m1_rne_satfinite(fabsf(__fdiv_rn(hi, dec))) << 4);
+        byte |= (__float_as_uint(lo) >> 31) << 3;
+        byte |= (__float_as_uint(hi) >> 31) << 7;
+        out[j >> 2] |= byte << (8 * (j & 3));
+    }
+    *reinterpret_cast<uint4*>(packed + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+    __threadfence();
+}
+
 cudaError_t launch_pack(const float* w, int N, int K, int kind, uint8_t* packed, void* scales,
                         float* tensor_scale, WsHeader* ws, int num_sms, cudaStream_t s) {
     cudaError_t err = cudaMemsetAsync(&ws->amax_bits, 0, sizeof(unsigned), s);
@@ -119,12 +164,20 @@ cudaError_t launch_pack(const float* w, int N, int K, int kind, uint8_t* packed,
     pack_amax_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(w), n4, ws);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (kind == NVFP4_SCALE_UE8M0) {
+        const size_t nb = n / 32;
+        pack_quant_ue8m0_kernel<<<(int)((nb + 255) / 256), 256, 0, s>>>(w, nb, packed, static_cast<uint8_t*>(scales),
+                                                                         tensor_scale);
+        return cudaGetLastError();
+    }
     const size_t nb = n / 16;
     const int qgrid = (int)((nb + 255) / 256);
     if (kind == NVFP4_SCALE_E4M3)
         pack_quant_kernel<NVFP4_SCALE_E4M3><<<qgrid, 256, 0, s>>>(w, nb, packed, scales, tensor_scale, ws);
-    else
+    else if (kind == NVFP4_SCALE_FP16)
         pack_quant_kernel<NVFP4_SCALE_FP16><<<qgrid, 256, 0, s>>>(w, nb, packed, scales, tensor_scale, ws);
+    else
+        pack_quant_kernel<NVFP4_SCALE_FP32><<<qgrid, 256, 0, s>>>(w, nb, packed, scales, tensor_scale, ws);
     return cudaGetLastError();
 }
 

@@ -90,7 +90,7 @@ def test_layer_argument_checks(nv):
         (_desc(nv, E=257), nv.NVFP4_ERR_UNSUPPORTED_SHAPE),
         (_desc(nv, H=2040), nv.NVFP4_ERR_UNSUPPORTED_SHAPE),
         (_desc(nv, I=500), nv.NVFP4_ERR_UNSUPPORTED_SHAPE),
-        (_desc(nv, kind=3), nv.NVFP4_ERR_INVALID_ARG),
+        (_desc(nv, kind=7), nv.NVFP4_ERR_INVALID_ARG),
         (_desc(nv, gu_packed=None), nv.NVFP4_ERR_INVALID_ARG),
         (_desc(nv, dn_scales=0x200004), nv.NVFP4_ERR_MISALIGNED),
         (_desc(nv, sh_gate_w=None), nv.NVFP4_ERR_INVALID_ARG),
@@ -105,3 +105,44 @@ def test_layer_argument_checks(nv):
         nv.NVFP4_ERR_INVALID_ARG
     assert lib.moe_layer_forward(ctypes.byref(d), ctypes.c_void_p(0x100002), 1, fake, None, None, fake, ws,
                                  None) == nv.NVFP4_ERR_MISALIGNED
+
+
+def test_residual_and_kind_argument_checks(nv):
+    """Host-side checks of moe_layer_forward_residual and of the scale-kind tag (nothing is
+    enqueued when a check fails, so no GPU is needed)."""
+    lib = nv.lib
+    fake = ctypes.c_void_p(0x100000)
+    d = _desc(nv)
+    ws = lib.moe_layer_residual_workspace_size(ctypes.byref(d), 1)
+    assert ws > lib.moe_layer_workspace_size(ctypes.byref(d), 1)
+    call = lambda dd, nw=fake, eps=1e-6, h=fake, out=fake, wsb=ws: lib.moe_layer_forward_residual(
+        ctypes.byref(dd), nw, eps, h, 1, out, None, None, fake, wsb, None)
+    assert call(d, nw=None) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(d, eps=-1.0) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(d, eps=float("nan")) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(d, nw=ctypes.c_void_p(0x100008)) == nv.NVFP4_ERR_MISALIGNED
+    assert call(d, wsb=16) == nv.NVFP4_ERR_WORKSPACE_TOO_SMALL
+    assert call(_desc(nv, kind=9)) == nv.NVFP4_ERR_INVALID_ARG
+    # pack: E8M0 blocks are 32 elements
+    assert lib.nvfp4_pack(fake, 4, 48, 3, fake, fake, fake, fake, 256, None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_pack(fake, 4, 48, 5, fake, fake, fake, fake, 256, None) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_scale_kind_classifier(nv):
+    """Metadata-only classification of the stored scale contract (README P59): every kind
+    is recognised from (count, element size), everything else is refused."""
+    import torch
+    N, K = 12, 256
+    cases = [((N, K // 16), torch.uint8, nv.SCALE_E4M3), ((N, K // 16), torch.int16, nv.SCALE_FP16),
+             ((N, K // 16), torch.float32, nv.SCALE_FP32), ((N, K // 32), torch.uint8, nv.SCALE_UE8M0)]
+    for shape, dt, want in cases:
+        assert nv.nvfp4_scale_kind_of(N, K, torch.empty(shape, dtype=dt)) == want
+        shp, sdt = nv.scale_shape(N, K, want)
+        assert tuple(shp) == shape and sdt == dt
+    for shape, dt in [((N, K // 32), torch.int16), ((N, K // 8), torch.uint8), ((N, K // 16 + 1), torch.uint8),
+                      ((N, K // 32), torch.float32)]:
+        with pytest.raises(nv.NVFP4Error):
+            nv.nvfp4_scale_kind_of(N, K, torch.empty(shape, dtype=dt))
+    # K = 48 has no per-32 reading
+    with pytest.raises(nv.NVFP4Error):
+        nv.nvfp4_scale_kind_of(4, 48, torch.empty(4, 1, dtype=torch.uint8))

@@ -75,3 +75,62 @@ def test_gemv_deterministic(nv):
     y0 = nv.nvfp4_gemv_w4a16(W, x)
     for _ in range(9):
         assert torch.equal(nv.nvfp4_gemv_w4a16(W, x), y0)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gemv_lm_head_vocab(nv, T):
+    """The NVFP4 lm_head of Qwen3.6-35B-A3B (lynn-engine tutorials index, Qwen 3.6 config
+    block: vocab_size 248320, hidden 2048) as one dense W4A16 GEMV, FP16 block scales
+    (the P1 stage's format; a row's bytes depend on that row only, so the oracle packs just
+    the rows it checks). 512 rows spread over the vocabulary, the first and the last, are
+    compared with the oracle; all rows must be finite."""
+    N, K, seed = 248320, 2048, 17
+    w = wl.dense_weight_f32(seed, N, K, device="cuda")
+    W = nv.nvfp4_pack(w, 1, check=True)
+    del w
+    x = wl.activations(seed, T, K)
+    y = nv.nvfp4_gemv_w4a16(W, x.cuda())
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 510, replace=False)]))
+    key = wl.stream_key(seed, 0, wl.K_DENSE)
+    wr = torch.stack([wl.normal(key, K, 0.02, start=int(r) * K) for r in rows])
+    ref = oracle.gemv(oracle.pack(wr, 1), x)
+    got = y.float().cpu().numpy().astype(np.float64)[:, rows]
+    ok, err, bound = tol_ok(got, ref)
+    assert ok, (err, bound)
+    assert err <= 2.0 ** -7 * np.abs(ref).max() + 1e-6
+
+
+def test_gemv_lm_head_e4m3_scales(nv):
+    """E4M3 block scales at a 32768-row vocabulary slice (the tensor scale depends on the whole
+    matrix, so the oracle packs all of it)."""
+    _run(nv, 32768, 2048, 1, 0, seed=18)
+
+
+@pytest.mark.parametrize("kind", [2, 3])
+@pytest.mark.parametrize("N,K,T", [(8192, 2048, 1), (301, 1024, 3), (77, 64, 9), (5000, 8192, 2)])
+def test_gemv_other_scale_contracts(nv, kind, N, K, T):
+    """FP32 per-16 and E8M0 per-32 block scales (README P52, P17/P18): packer bytes and scales
+    bit-exact against the oracle's, GEMV within the bar."""
+    w = wl.dense_weight_f32(50 + kind, N, K)
+    W = nv.nvfp4_pack(w.cuda(), kind, check=True)
+    ref_p = oracle.pack(w, kind)
+    assert np.array_equal(W.packed.cpu().numpy(), ref_p.packed)
+    gs = W.scales.cpu().numpy().view(ref_p.scales.dtype)
+    assert np.array_equal(gs, ref_p.scales)
+    assert float(W.tensor_scale.cpu()[0]) == ref_p.tensor_scale == 1.0
+    x = wl.activations(50 + kind, T, K)
+    y = nv.nvfp4_gemv_w4a16(W, x.cuda())
+    torch.cuda.synchronize()
+    ok, err, bound = tol_ok(y.float().cpu().numpy().astype(np.float64), oracle.gemv(ref_p, x))
+    assert ok, (err, bound)
+
+
+def test_gemv_ue8m0_needs_k_multiple_of_64(nv):
+    w = wl.dense_weight_f32(60, 16, 96)
+    W = nv.nvfp4_pack(w.cuda(), 3)
+    with pytest.raises(nv.NVFP4Error) as ei:
+        nv.nvfp4_gemv_w4a16(W, wl.activations(60, 1, 96).cuda())
+    assert ei.value.status == nv.NVFP4_ERR_UNSUPPORTED_SHAPE

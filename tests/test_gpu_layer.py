@@ -116,3 +116,17 @@ def test_workspace_too_small(nv):
     with pytest.raises(nv.NVFP4Error) as ei:
         nv.moe_layer_forward(layer, wl.activations(0, 1, 256).cuda(), ws=ws)
     assert ei.value.status == nv.NVFP4_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("kind", [2, 3])
+@pytest.mark.parametrize("T", [1, 6])
+def test_layer_other_scale_contracts(nv, kind, T):
+    """A layer stored with FP32 per-16 or E8M0 per-32 scales runs on the fp32 multi-token
+    kernels (the fast paths take E4M3 / FP16 only and refuse nothing silently)."""
+    shape = wl.MoEShape(H=512, E=32, k=4, I=256, Is=256)
+    L = wl.LayerInputs(shape, seed=60 + kind)
+    layer = gpu_layer(L, kind=kind)
+    x = wl.activations(60 + kind, T, 512)
+    y, ids, w = _forward(nv, layer, x)
+    check_layer_parity(L, x, y, ids, w, kind=kind)
+    assert nv.launches_per_layer_call(T, 512, kind=kind, E=32, I=256, Is=256, k=4) == 5
