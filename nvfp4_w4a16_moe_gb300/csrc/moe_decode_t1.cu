@@ -82,13 +82,13 @@ struct T1Params {
     float eps;
     const uint16_t* resid;        // nullable: y = bf16(resid + layer)
     // shared-memory layout (bytes), identical for every CTA
-    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_h16;
+    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_dns, o_h16;
     uint32_t sg_reg;      // bytes of one region of the shared-pair area (codes)
     uint32_t sg_sreg;     // ... (scales)
     uint32_t gu_reg;      // bytes of one region of the routed-pair area (codes)
     uint32_t gu_sreg;     // ... (scales)
-    uint32_t dn_slot;     // bytes of one slot of the down area (codes, then scales)
-    uint32_t dn_sc;       // offset of the scales inside a down slot
+    uint32_t dn_row;      // bytes of one down row over all slots: (k*I + Is) / 2
+    uint32_t dn_srow;     // ... of its scales: (k*I + Is) / 16 * scale bytes
     unsigned long long mG64;   // ceil(2^64 / G)
 };
 
@@ -182,22 +182,45 @@ __device__ __forceinline__ void scales2(const uint8_t* srow, int s, float& s0, f
     }
 }
 
-// One 16-byte segment (32 codes, two scale blocks) against 32 f16 activations stored
-// segment-interleaved (unit c of segment s at c * nseg + s).
-template <int KIND>
-__device__ __forceinline__ float seg_dot(const uint4 w, float s0, float s1, const uint4* xv, int nseg, int s) {
+// One 16-byte segment (32 codes, two scale blocks) against its 32 f16 activations (four
+// units of eight).
+__device__ __forceinline__ float seg_dot_r(const uint4 w, float s0, float s1, const uint4 u0, const uint4 u1,
+                                           const uint4 u2, const uint4 u3) {
     uint32_t a[4], b[4], c[4], d[4];
     expand4(w.x, a);
     expand4(w.y, b);
     expand4(w.z, c);
     expand4(w.w, d);
-    const uint4 u0 = xv[s], u1 = xv[nseg + s], u2 = xv[2 * nseg + s], u3 = xv[3 * nseg + s];
     float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
     p0 = fma2h(a[0], u0.x, p0); p1 = fma2h(a[1], u0.y, p1); p0 = fma2h(a[2], u0.z, p0); p1 = fma2h(a[3], u0.w, p1);
     p0 = fma2h(b[0], u1.x, p0); p1 = fma2h(b[1], u1.y, p1); p0 = fma2h(b[2], u1.z, p0); p1 = fma2h(b[3], u1.w, p1);
     p2 = fma2h(c[0], u2.x, p2); p3 = fma2h(c[1], u2.y, p3); p2 = fma2h(c[2], u2.z, p2); p3 = fma2h(c[3], u2.w, p3);
     p2 = fma2h(d[0], u3.x, p2); p3 = fma2h(d[1], u3.y, p3); p2 = fma2h(d[2], u3.z, p2); p3 = fma2h(d[3], u3.w, p3);
     return fmaf(s0, p0 + p1, s1 * (p2 + p3));
+}
+
+// The same with the activations stored segment-interleaved (unit c of segment s at c * nseg + s).
+template <int KIND>
+__device__ __forceinline__ float seg_dot(const uint4 w, float s0, float s1, const uint4* xv, int nseg, int s) {
+    return seg_dot_r(w, s0, s1, xv[s], xv[nseg + s], xv[2 * nseg + s], xv[3 * nseg + s]);
+}
+
+// Sum of each of v[0..7] over the warp, spread over the lanes: lane l ends with the sum of
+// v[(l >> 2) & 7] (halving exchanges at distances 16, 8, 4, then the quad; 9 shuffles, a
+// fixed order).
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w4[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 4], 16);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        w2[j] = (b3 ? w4[j + 2] : w4[j]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[j] : w4[j + 2], 8);
+    float z = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    return z;
 }
 
 // (gate . x, up . x) of one pair whose rows sit in shared memory; lanes over segments.
@@ -250,14 +273,15 @@ __device__ __forceinline__ uint32_t copy_range(uint8_t* dst, const uint8_t* src,
 template <int KIND>
 __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
     extern __shared__ __align__(128) uint8_t sm[];
-    __shared__ uint64_t mbA, mbS, mbB[kChunks];
+    __shared__ uint64_t mbA, mbB[kChunks];
     __shared__ int s_ids[NVFP4_MAX_TOPK];
-    __shared__ float s_coef[kSlots];                       // down coefficient of each slot
+    __shared__ float s_coef[kSlots];       // slot weight times the down tensor scale
     __shared__ float s_tsg[kSlots], s_tsu[kSlots];
-    __shared__ uint32_t s_hmax[kSlots];
+    __shared__ uint32_t s_hm;              // max over slots of |h| |coef| (fp32 bits)
     __shared__ uint32_t s_xmax, s_tag;
     __shared__ int s_fail;
     __shared__ float s_ss[kThr / 32];
+    __shared__ float s_red[2][kW][8];       // routed-pair sums of each warp, per batch parity
     __shared__ float s_tg[NVFP4_MAX_EXPERTS * 2], s_td[NVFP4_MAX_EXPERTS];   // every expert's tensor scales
 
     const moe_layer_desc& d = P.d;
@@ -289,18 +313,20 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
     uint8_t* RT = sm + P.o_rt;
     uint8_t* SG = sm + P.o_sg;                // regions: gate codes, up codes, gate scales, up scales
     uint8_t* GU = sm + P.o_gu;                // same four regions for the routed pairs
-    uint8_t* DN = sm + P.o_dn;                // slot j: codes [nN][I/2], then scales [nN][I/16*sb]
+    // down rows of the CTA's outputs over all k + 1 slots: row nl holds slot j's codes at
+    // j * I/2 (shared slot at k * I/2), its scales likewise in the scale region
+    uint8_t* DN = sm + P.o_dn;
+    uint8_t* DNs = sm + P.o_dns;
     uint4* h16 = reinterpret_cast<uint4*>(sm + P.o_h16);
 
     // ------------------------------------------------------------------ prologue
     if (tid == 0) {
         mbar_init(&mbA, 1);
-        mbar_init(&mbS, 1);
         for (int i = 0; i < kChunks; ++i) mbar_init(&mbB[i], 1);
         fence_mbar_init();
         s_fail = 0;
         s_xmax = 0u;
-        for (int j = 0; j < kSlots; ++j) s_hmax[j] = 0u;
+        s_hm = 0u;
     }
     __syncthreads();
     const uint8_t* sh_gu = d.sh_gu_packed;
@@ -312,7 +338,6 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
             const uint32_t a = (uint32_t)(min(nR1, E) - min(nR0, E)) * 2u * H + (nR1 > E ? 2u * H : 0u) +
                                (uint32_t)nS * 2u * (rowH + srowH);
             mbar_arrive_expect_tx(&mbA, a);
-            mbar_arrive_expect_tx(&mbS, Is > 0 ? (uint32_t)nN * (rowS + srowS) : 0u);
         }
         __syncwarp();
         const int rE = min(nR1, E) - min(nR0, E);   // router rows of this CTA below E
@@ -327,13 +352,23 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
             if (lane == 5)
                 copy_range(SG + 2 * P.sg_reg + P.sg_sreg, sh_gus + (size_t)(Is + s0) * srowH, (uint32_t)nS * srowH, &mbA);
         }
-        if (Is > 0) {
-            uint8_t* dsl = DN + (size_t)k * P.dn_slot;
-            if (lane == 6) copy_range(dsl, d.sh_dn_packed + (size_t)n0 * rowS, (uint32_t)nN * rowS, &mbS);
-            if (lane == 7)
-                copy_range(dsl + P.dn_sc, static_cast<const uint8_t*>(d.sh_dn_scales) + (size_t)n0 * srowS,
-                           (uint32_t)nN * srowS, &mbS);
+    } else if (Is > 0) {
+        // the shared expert's down rows of this CTA's outputs, 16 bytes per cp.async, into
+        // the shared slot of each row
+        const int pr = (int)(rowS >> 4), ps = (int)(srowS >> 4);
+        const uint32_t rowI_ = I / 2, srowI_ = I / 16 * sb;
+        for (int i = tid; i < nN * (pr + ps); i += kW * 32) {
+            if (i < nN * pr) {
+                const int nl = i / pr, q = i - nl * pr;
+                cp_async16(DN + (size_t)nl * P.dn_row + (size_t)k * rowI_ + 16 * q,
+                           d.sh_dn_packed + (size_t)n0 * rowS + 16 * (size_t)i);
+            } else {
+                const int r = i - nN * pr, nl = r / ps, q = r - nl * ps;
+                cp_async16(DNs + (size_t)nl * P.dn_srow + (size_t)k * srowI_ + 16 * q,
+                           static_cast<const uint8_t*>(d.sh_dn_scales) + (size_t)n0 * srowS + 16 * (size_t)r);
+            }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
     // every expert's tensor scales (read after the top-k): requested now into registers, written
@@ -352,20 +387,26 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
         sh_tsd = __ldg(d.sh_dn_tscale);
     }
 
+    // this launch's tag. The atomic is issued before griddepcontrol.wait (its latency hides
+    // behind the wait and the x load): a dependent launch starts only after every CTA of
+    // this one has passed launch_dependents, which comes after this atomic, so the counts
+    // of consecutive launches never interleave
+    unsigned long long n_start = 0;
+    if (tid == 0)
+        asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n_start) : "l"(&P.hdr->barrier) : "memory");
+
     // everything below may read what the previous kernel on the stream wrote
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    if (tid == 0) {
-        unsigned long long n;
-        asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(n) : "l"(&P.hdr->barrier) : "memory");
-        unsigned long long q = __umul64hi(n, P.mG64);    // n / G, corrected below
-        if ((q + 1) * (unsigned long long)G <= n) ++q;
-        if (q * (unsigned long long)G > n) --q;
-        s_tag = (uint32_t)q + 1u;
-    }
     // x: raw bf16 for the router, and max |x| for the f16 copy
     uint4 xv = make_uint4(0, 0, 0, 0);
     if (tid < nunitH) xv = reinterpret_cast<const uint4*>(P.x)[tid];
+    if (tid == 0) {   // the atomic's result is first used here, after the wait and the x load
+        unsigned long long q = __umul64hi(n_start, P.mG64);    // n / G, corrected below
+        if ((q + 1) * (unsigned long long)G <= n_start) ++q;
+        if (q * (unsigned long long)G > n_start) --q;
+        s_tag = (uint32_t)q + 1u;
+    }
     if (P.norm_w) {
         // pre-MoE RMSNorm (1 + w) x / sqrt(mean(x^2) + eps): squares summed per thread, per
         // warp by shuffles, then over the warps in a fixed order; rounded once to bf16
@@ -469,43 +510,53 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
     __syncthreads();
     if (s_fail) {
         if (tid == 0) record_status(P.hdr, NVFP4_ERR_DEVICE_TIMEOUT);
-        if (tid == 0) {
-            mbar_wait_bounded(&mbA, 0, kDefaultWaitLimit);
-            mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit);
-        }
+        if (tid == 0) mbar_wait_bounded(&mbA, 0, kDefaultWaitLimit);
+        if (warp < kW) asm volatile("cp.async.wait_all;" ::: "memory");
         return;
     }
 
     // ------------------------------------------------------------------ top-k
     if (warp == 0) {
-        uint32_t key[8];
+        // lane l holds experts 8l .. 8l+7 as 64-bit keys (order key, then 7 - i so that the
+        // lower id wins ties), sorted descending in registers by an odd-even merge network;
+        // each round the warp takes the largest head (the lowest lane among equal heads
+        // holds the lowest id) and the lane that held it drops it
+        unsigned long long kk[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) key[i] = lane + 32 * i < E ? order_key(lg[lane + 32 * i]) : 0u;
+        for (int i = 0; i < 8; ++i) {
+            const int e = 8 * lane + i;
+            kk[i] = e < E ? ((unsigned long long)order_key(lg[e]) << 3) | (unsigned)(7 - i) : 0ull;
+        }
+#define T1_CX(a, b) { const unsigned long long hi_ = max(kk[a], kk[b]), lo_ = min(kk[a], kk[b]); kk[a] = hi_; kk[b] = lo_; }
+        T1_CX(0, 1) T1_CX(2, 3) T1_CX(4, 5) T1_CX(6, 7)
+        T1_CX(0, 2) T1_CX(1, 3) T1_CX(4, 6) T1_CX(5, 7)
+        T1_CX(1, 2) T1_CX(5, 6)
+        T1_CX(0, 4) T1_CX(1, 5) T1_CX(2, 6) T1_CX(3, 7)
+        T1_CX(2, 4) T1_CX(3, 5)
+        T1_CX(1, 2) T1_CX(3, 4) T1_CX(5, 6)
+#undef T1_CX
         int my_id = -1;
         float ex = 0.f, vmax = 0.f;
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
-            uint32_t best = key[0];
-            int bi = 0;
+            const uint32_t hk = (uint32_t)(kk[0] >> 3);
+            const uint32_t wb = __reduce_max_sync(0xffffffffu, hk);
+            const int win = __ffs(__ballot_sync(0xffffffffu, hk == wb)) - 1;
+            const int e = __shfl_sync(0xffffffffu, 8 * lane + 7 - (int)((uint32_t)kk[0] & 7u), win);
+            if (lane == win) {
 #pragma unroll
-            for (int i = 1; i < 8; ++i)
-                if (key[i] > best) { best = key[i]; bi = i; }   // strict: the lower id wins ties
-            const uint32_t wb = __reduce_max_sync(0xffffffffu, best);
-            const uint32_t e = __reduce_min_sync(0xffffffffu, best == wb ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
-            if ((int)(e & 31) == lane) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i == bi) key[i] = 0u;
+                for (int i = 0; i < 7; ++i) kk[i] = kk[i + 1];
+                kk[7] = 0ull;
             }
             const float v = key_value(wb);
             if (j == 0) vmax = v;
-            if (lane == j) { my_id = (int)e; ex = __expf(v - vmax); }
+            if (lane == j) { my_id = e; ex = __expf(v - vmax); }
         }
         const float sum = warp_sum(lane < k ? ex : 0.f);
         if (lane < k) {
             const float wj = __fdividef(ex, sum);
             s_ids[lane] = my_id;
-            s_coef[lane] = wj;
+            s_coef[lane] = wj * s_td[my_id];
             s_tsg[lane] = s_tg[2 * my_id];
             s_tsu[lane] = s_tg[2 * my_id + 1];
             if (c == 0) {
@@ -559,31 +610,71 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
             for (int i = tid; i < k * per_slot; i += kW * 32) {
                 const int j = i / per_slot, r = i - j * per_slot;
                 const size_t rb = (size_t)s_ids[j] * H + n0;
-                uint8_t* dsl = DN + (size_t)j * P.dn_slot;
                 if (r < nN * pr) {
-                    cp_async16(dsl + 16 * (size_t)r, d.dn_packed + rb * rowI + 16 * (size_t)r);
+                    const int nl = r / pr, q = r - nl * pr;
+                    cp_async16(DN + (size_t)nl * P.dn_row + (size_t)j * rowI + 16 * q,
+                               d.dn_packed + rb * rowI + 16 * (size_t)r);
                 } else {
-                    const int q = r - nN * pr;
-                    cp_async16(dsl + P.dn_sc + 16 * (size_t)q,
-                               static_cast<const uint8_t*>(d.dn_scales) + rb * srowI + 16 * (size_t)q);
+                    const int r2 = r - nN * pr, nl = r2 / ps, q = r2 - nl * ps;
+                    cp_async16(DNs + (size_t)nl * P.dn_srow + (size_t)j * srowI + 16 * q,
+                               static_cast<const uint8_t*>(d.dn_scales) + rb * srowI + 16 * (size_t)r2);
                 }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
         // ---------------------------------------------------------------- routed pairs
-        for (int r = warp; r < nq; r += kW) {
-            int ch = 0;
-            while (ch + 1 < kChunks && r >= nq * (ch + 1) / kChunks) ++ch;
-            if (ok && !mbar_wait_bounded(&mbB[ch], 0, kDefaultWaitLimit)) ok = false;
-            if (!ok) break;
-            const float m = pair_dot<KIND>(GU + (size_t)r * rowH, GU + P.gu_reg + (size_t)r * rowH,
-                                           GU + 2 * P.gu_reg + (size_t)r * srowH,
-                                           GU + 2 * P.gu_reg + P.gu_sreg + (size_t)r * srowH, x16, nsegH, lane);
-            const float gsum = __shfl_sync(0xffffffffu, m, 0), usum = __shfl_sync(0xffffffffu, m, 16);
-            if (lane < kWordReplicas) {
-                const int q = q0 + r, j = q / I;
-                const float hv = silu_f32(gsum * inv_x * s_tsg[j]) * (usum * inv_x * s_tsu[j]);
-                st_hword(w_h_all + lane * h_stride + q, tag16, hv);
+        // lane group g (warps 2g, 2g + 1) takes local pairs g, g + 8, g + 16, ... in batches of
+        // four, its lane i the segments i, i + 64, ... of H. A lane holds its x segment in
+        // registers across the batch and keeps a gate and an up sum per pair; each warp reduces
+        // its 8 sums (warp_sum8), and the group adds its two warps' sums in a fixed order.
+        {
+            constexpr int kGroups = kW / 2, kBatch = 4;
+            const int g = warp >> 1, gi = tid & 63;
+            const int npg = nq > g ? (nq - g + kGroups - 1) / kGroups : 0;   // pairs of group g
+            const uint8_t* GUs = GU + 2 * P.gu_reg;
+            for (int b = 0; b * kBatch < npg; ++b) {
+                float v[2 * kBatch];
+#pragma unroll
+                for (int i = 0; i < 2 * kBatch; ++i) v[i] = 0.f;
+                for (int s = gi; s < nsegH; s += 64) {
+                    const uint4 u0 = x16[s], u1 = x16[nsegH + s], u2 = x16[2 * nsegH + s], u3 = x16[3 * nsegH + s];
+#pragma unroll
+                    for (int m = 0; m < kBatch; ++m) {
+                        const int n = b * kBatch + m;
+                        if (n < npg) {
+                            const int r = g + kGroups * n;
+                            int ch = 0;
+                            while (ch + 1 < kChunks && r >= nq * (ch + 1) / kChunks) ++ch;
+                            if (ok && !mbar_wait_bounded(&mbB[ch], 0, kDefaultWaitLimit)) ok = false;
+                            if (ok) {
+                                float g0, g1, a0, a1;
+                                scales2<KIND>(GUs + (size_t)r * srowH, s, g0, g1);
+                                scales2<KIND>(GUs + P.gu_sreg + (size_t)r * srowH, s, a0, a1);
+                                v[2 * m] += seg_dot_r(reinterpret_cast<const uint4*>(GU + (size_t)r * rowH)[s],
+                                                      g0, g1, u0, u1, u2, u3);
+                                v[2 * m + 1] += seg_dot_r(
+                                    reinterpret_cast<const uint4*>(GU + P.gu_reg + (size_t)r * rowH)[s], a0, a1,
+                                    u0, u1, u2, u3);
+                            }
+                        }
+                    }
+                }
+                const float z = warp_sum8(v, lane);
+                if ((lane & 3) == 0) s_red[b & 1][warp][(lane >> 2) & 7] = z;
+                named_sync(2 + g, 64);
+                if ((warp & 1) == 0 && ok) {
+                    // lane = m * kWordReplicas + copy: pair m of the batch, one replica each
+                    for (int i = lane; i < kBatch * kWordReplicas; i += 32) {
+                        const int m = i / kWordReplicas, cp = i - m * kWordReplicas, n = b * kBatch + m;
+                        if (n < npg) {
+                            const int q = q0 + g + kGroups * n, j = q / I;
+                            const float gs = s_red[b & 1][warp][2 * m] + s_red[b & 1][warp + 1][2 * m];
+                            const float us = s_red[b & 1][warp][2 * m + 1] + s_red[b & 1][warp + 1][2 * m + 1];
+                            const float hv = silu_f32(gs * inv_x * s_tsg[j]) * (us * inv_x * s_tsu[j]);
+                            st_hword(w_h_all + cp * h_stride + q, tag16, hv);
+                        }
+                    }
+                }
             }
         }
         // ---------------------------------------------------------------- gather h
@@ -619,7 +710,8 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
                 }
             }
         }
-        // per-slot maxima (a warp's 256 consecutive words lie in one slot: I % 256 == 0)
+        // max of |h| |coef_j| over all slots (a warp's 256 consecutive words lie in one
+        // slot: I % 256 == 0)
 #pragma unroll
         for (int u = 0; u < kMaxU; ++u) {
             const int base = 8 * (warp * 32 + u * kW * 32);   // first word of this warp's 256
@@ -628,39 +720,38 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
                 uint32_t m = max(max(a.x & 0x7FFFu, a.y & 0x7FFFu), max(a.z & 0x7FFFu, a.w & 0x7FFFu));
                 m = max(m, max(max(b.x & 0x7FFFu, b.y & 0x7FFFu), max(b.z & 0x7FFFu, b.w & 0x7FFFu)));
                 m = __reduce_max_sync(0xffffffffu, m);
-                if (lane == 0) atomicMax(&s_hmax[base < total ? base / I : k], m << 16);
+                if (lane == 0)
+                    atomicMax(&s_hm, __float_as_uint(__uint_as_float(m << 16) * fabsf(s_coef[base < total ? base / I : k])));
             }
         }
         named_sync(1, kW * 32);
-        // slot j's values as f16 times 2^sh_j, segment-interleaved per slot; a unit's eight
-        // consecutive elements are one 16-byte store
+        // coef_j h as f16 times 2^sh (max in [2^14, 2^15)), the k + 1 slots as one vector of
+        // nsegT 32-element segments, segment-interleaved; a unit of eight consecutive
+        // elements is one 16-byte store
+        const int nsegT = nh >> 5;
+        const float s2 = exp2_int(pow2_shift(s_hm));
 #pragma unroll
         for (int u = 0; u < kMaxU; ++u) {
             const int i = tid + u * kW * 32;
             if (i < nu && ok) {
                 const int e0 = 8 * i;
-                const int j = e0 < total ? e0 / I : k;
-                const int e = e0 < total ? e0 - j * I : e0 - total;
-                const int K = j < k ? I : Is;
-                const float sc = exp2_int(pow2_shift(s_hmax[j]));
+                const float sc = s_coef[e0 < total ? e0 / I : k] * s2;
                 const uint4 a = wa[u], b = wb[u];
                 const uint4 o = make_uint4(to_f16x2(bf16lo(a.x) * sc, bf16lo(a.y) * sc),
                                            to_f16x2(bf16lo(a.z) * sc, bf16lo(a.w) * sc),
                                            to_f16x2(bf16lo(b.x) * sc, bf16lo(b.y) * sc),
                                            to_f16x2(bf16lo(b.z) * sc, bf16lo(b.w) * sc));
-                const int u8 = e >> 3, nseg = K >> 5;
-                h16[(size_t)j * (I >> 3) + (u8 & 3) * nseg + (u8 >> 2)] = o;
+                h16[((e0 >> 3) & 3) * nsegT + (e0 >> 5)] = o;
             }
         }
     }
     if (warp < kW) asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's down-row pieces
     if (!ok) s_fail = 1;
     __syncthreads();
-    if (s_fail || !mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit)) {
+    if (s_fail) {
         if (tid == 0) {
             record_status(P.hdr, NVFP4_ERR_DEVICE_TIMEOUT);
             for (int i = 0; i < kChunks; ++i) mbar_wait_bounded(&mbB[i], 0, kDefaultWaitLimit);
-            mbar_wait_bounded(&mbS, 0, kDefaultWaitLimit);
         }
         return;
     }
@@ -670,40 +761,21 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
 
     // ------------------------------------------------------------------ down
     if (warp < kW) {
-        const int nsegI = I >> 5, nsegS = Is >> 5;
-        const int work = k * nsegI + nsegS;
-        float coef[kSlots];
-#pragma unroll
-        for (int j = 0; j < kSlots; ++j) {
-            coef[j] = 0.f;
-            if (j < k) coef[j] = s_coef[j] * s_td[s_ids[j]] * exp2_int(-pow2_shift(s_hmax[j]));
-            else if (j == k && Is > 0) coef[j] = s_coef[k] * exp2_int(-pow2_shift(s_hmax[k]));
-        }
+        const int nsegT = (total + Is) >> 5;
+        const float inv_h = exp2_int(-pow2_shift(s_hm));
         for (int nl = warp; nl < nN; nl += kW) {
-            // lane l sums the weighted segments l, l + 32, ... of the (slot, segment) list in
-            // that order, then the warp is reduced once: a fixed order, no atomics
+            // lane l sums segments l, l + 32, ... of the row in that order, then the warp is
+            // reduced once: a fixed order, no atomics
+            const uint8_t* wr = DN + (size_t)nl * P.dn_row;
+            const uint8_t* sr = DNs + (size_t)nl * P.dn_srow;
             float acc = 0.f;
-            int j = 0, s = lane;               // (slot, segment) of item p = lane + 32 m
-            while (j < k && s >= nsegI) { s -= nsegI; ++j; }
 #pragma unroll 1
-            for (int p = lane; p < work; p += 32) {
-                if (j == k && s >= nsegS) break;
-                const int K = j < k ? I : Is;
-                const uint32_t rb = K / 2, srb = K / 16 * sb;
-                const uint8_t* dsl = DN + (size_t)j * P.dn_slot;
+            for (int S = lane; S < nsegT; S += 32) {
                 float sa, sb2;
-                scales2<KIND>(dsl + P.dn_sc + (size_t)nl * srb, s, sa, sb2);
-                const float v = seg_dot<KIND>(reinterpret_cast<const uint4*>(dsl + (size_t)nl * rb)[s], sa, sb2,
-                                              h16 + (size_t)j * (I >> 3), K >> 5, s);
-                float cj = 0.f;
-#pragma unroll
-                for (int jj = 0; jj < kSlots; ++jj)
-                    if (jj == j) cj = coef[jj];
-                acc = fmaf(cj, v, acc);
-                s += 32;
-                while (j < k && s >= nsegI) { s -= nsegI; ++j; }
+                scales2<KIND>(sr, S, sa, sb2);
+                acc += seg_dot<KIND>(reinterpret_cast<const uint4*>(wr)[S], sa, sb2, h16, nsegT, S);
             }
-            acc = warp_sum(acc);
+            acc = warp_sum(acc) * inv_h;
             if (lane == 0) {
                 if (P.resid) acc += bf16_to_f32(P.resid[n0 + nl]);   // residual stream, before the rounding
                 P.y[n0 + nl] = f32_to_bf16(acc);
@@ -713,8 +785,8 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
 }
 
 struct T1Layout {
-    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_h16, total;
-    uint32_t sg_reg, sg_sreg, gu_reg, gu_sreg, dn_slot, dn_sc;
+    uint32_t o_xb, o_x16, o_lg, o_rt, o_sg, o_gu, o_dn, o_dns, o_h16, total;
+    uint32_t sg_reg, sg_sreg, gu_reg, gu_sreg, dn_row, dn_srow;
 };
 
 uint32_t a16(size_t v) { return (uint32_t)((v + 15) & ~size_t(15)); }
@@ -724,14 +796,14 @@ T1Layout t1_layout(const moe_layer_desc& d, int G) {
     const size_t H = d.H, I = d.I, Is = d.Is, k = d.k, E = d.E;
     const size_t nR = (E + 1 + G - 1) / G + 1, nS = (Is + G - 1) / G + 1;
     const size_t nq = (k * I + G - 1) / G + 1, nN = (H + G - 1) / G + 1;
-    const size_t Im = I > Is ? I : Is;
+    const size_t KT = k * I + Is;             // the k + 1 slots as one vector
     T1Layout L;
     L.sg_reg = a16(nS * (H / 2));
     L.sg_sreg = a16(nS * (H / 16 * sb));
     L.gu_reg = a16(nq * (H / 2));
     L.gu_sreg = a16(nq * (H / 16 * sb));
-    L.dn_sc = a16(nN * (Im / 2));
-    L.dn_slot = L.dn_sc + a16(nN * (Im / 16 * sb));
+    L.dn_row = (uint32_t)(KT / 2);
+    L.dn_srow = (uint32_t)(KT / 16 * sb);
     size_t off = 0;
     L.o_xb = (uint32_t)off; off += a16(H * 2);
     L.o_x16 = (uint32_t)off; off += a16(H * 2);
@@ -739,8 +811,9 @@ T1Layout t1_layout(const moe_layer_desc& d, int G) {
     L.o_rt = (uint32_t)off; off += a16(nR * H * 2);
     L.o_sg = (uint32_t)off; off += 2 * (size_t)L.sg_reg + 2 * (size_t)L.sg_sreg;
     L.o_gu = (uint32_t)off; off += 2 * (size_t)L.gu_reg + 2 * (size_t)L.gu_sreg;
-    L.o_dn = (uint32_t)off; off += (size_t)L.dn_slot * (k + 1);
-    L.o_h16 = (uint32_t)off; off += a16((k + 1) * Im * 2);
+    L.o_dn = (uint32_t)off; off += a16(nN * (size_t)L.dn_row);
+    L.o_dns = (uint32_t)off; off += a16(nN * (size_t)L.dn_srow);
+    L.o_h16 = (uint32_t)off; off += a16(KT * 2);
     L.total = (uint32_t)off;
     return L;
 }
@@ -782,13 +855,14 @@ cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, 
     P.o_sg = L.o_sg;
     P.o_gu = L.o_gu;
     P.o_dn = L.o_dn;
+    P.o_dns = L.o_dns;
     P.o_h16 = L.o_h16;
     P.sg_reg = L.sg_reg;
     P.sg_sreg = L.sg_sreg;
     P.gu_reg = L.gu_reg;
     P.gu_sreg = L.gu_sreg;
-    P.dn_slot = L.dn_slot;
-    P.dn_sc = L.dn_sc;
+    P.dn_row = L.dn_row;
+    P.dn_srow = L.dn_srow;
     P.mG64 = ~0ull / (unsigned long long)G + 1ull;
     auto kern = d.kind == NVFP4_SCALE_E4M3 ? moe_decode_t1_kernel<NVFP4_SCALE_E4M3>
                                            : moe_decode_t1_kernel<NVFP4_SCALE_FP16>;
