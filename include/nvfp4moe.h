@@ -333,6 +333,31 @@ NVFP4_API nvfp4_status nvfp4_get_device_status(void* workspace, int32_t clear, v
  * waiting blocks then record NVFP4_ERR_DEVICE_TIMEOUT and return. */
 NVFP4_API void nvfp4_set_device_wait_limit(uint64_t limit_ns);
 
+/* Which kernel runs a single-token (T = 1) layer call (process-wide, default 0).
+ *   0  automatic: the persistent-grid form
+ *   1  the persistent-grid form (one CTA per SM; the logits and the SwiGLU values are
+ *      exchanged through global memory as tagged words)
+ *   2  the cluster form where the shape allows it (I and Is in {256, 512, 1024}, E4M3 or
+ *      FP16 scales, H <= 4096) and the device holds k clusters of 16, 12 or 8 CTAs at
+ *      once (k clusters, one per routed slot; the logits and the slot's SwiGLU values are
+ *      exchanged in distributed shared memory, the partial outputs through global
+ *      memory); otherwise the persistent-grid form. On GB300 it runs with 12-CTA clusters
+ *      on 96 SMs and measures slower than the grid form.
+ * Both compute the same result within the layer's tolerance; neither changes the API's
+ * arguments, workspace size or errors. Other values are taken as 0. */
+NVFP4_API void nvfp4_set_single_token_form(int32_t form);
+
+/* Which kernel a moe_layer_forward call of `T` tokens on layer `d` runs on the current
+ * device under the current setting: 2 the cluster form, 1 the persistent-grid form,
+ * 0 neither (multi-token kernels), -1 an invalid descriptor or no device. */
+NVFP4_API int32_t nvfp4_single_token_form_used(const moe_layer_desc* d, int32_t T);
+
+/* The cluster form's shape on the current device for layer `d`: 100 * cs + n, where cs
+ * is the cluster size it uses (16, 12 or 8 CTAs: the largest whose layout fits and of
+ * which the device holds k clusters at once) and n how many such clusters fit; 0 if the
+ * layer has no cluster form here, -1 on error. */
+NVFP4_API int32_t nvfp4_single_token_cluster_capacity(const moe_layer_desc* d);
+
 NVFP4_API const char* nvfp4_status_string(nvfp4_status s);
 NVFP4_API int32_t nvfp4_version(void);
 

@@ -126,6 +126,12 @@ lib.nvfp4_get_device_status.restype = _i32
 lib.nvfp4_get_device_status.argtypes = [_P, _i32, _P]
 lib.nvfp4_set_device_wait_limit.restype = None
 lib.nvfp4_set_device_wait_limit.argtypes = [ctypes.c_uint64]
+lib.nvfp4_set_single_token_form.restype = None
+lib.nvfp4_set_single_token_form.argtypes = [ctypes.c_int32]
+lib.nvfp4_single_token_form_used.restype = ctypes.c_int32
+lib.nvfp4_single_token_form_used.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+lib.nvfp4_single_token_cluster_capacity.restype = ctypes.c_int32
+lib.nvfp4_single_token_cluster_capacity.argtypes = [ctypes.c_void_p]
 lib.nvfp4_status_string.restype = ctypes.c_char_p
 lib.nvfp4_status_string.argtypes = [_i32]
 lib.nvfp4_version.restype = _i32
@@ -428,6 +434,29 @@ def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, y: Optional[torc
 
 def set_device_wait_limit(spins: int):
     lib.nvfp4_set_device_wait_limit(int(spins))
+
+
+SINGLE_TOKEN_AUTO = 0
+SINGLE_TOKEN_GRID = 1
+SINGLE_TOKEN_CLUSTER = 2
+
+
+def set_single_token_form(form: int):
+    """0: automatic (the persistent-grid form), 1: the grid form, 2: the cluster form
+    where supported."""
+    lib.nvfp4_set_single_token_form(int(form))
+
+
+def single_token_form_used(layer: "MoELayer", T: int = 1) -> int:
+    """2: the cluster form runs a T-token call of this layer, 1: the grid form, 0: neither."""
+    d = layer.desc()
+    return int(lib.nvfp4_single_token_form_used(ctypes.byref(d), int(T)))
+
+
+def single_token_cluster_capacity(layer: "MoELayer") -> int:
+    """Resident 16-CTA clusters of the cluster form on this device for this layer."""
+    d = layer.desc()
+    return int(lib.nvfp4_single_token_cluster_capacity(ctypes.byref(d)))
 
 
 def version() -> int:

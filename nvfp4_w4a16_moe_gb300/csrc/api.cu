@@ -277,6 +277,22 @@ nvfp4_status nvfp4_get_device_status(void* workspace, int32_t clear, void* strea
     return static_cast<nvfp4_status>(code);
 }
 
+void nvfp4_set_single_token_form(int32_t form) { set_t1_form(form == 1 || form == 2 ? form : 0); }
+
+int32_t nvfp4_single_token_form_used(const moe_layer_desc* d, int32_t T) {
+    if (!d || check_layer(d) != NVFP4_OK) return -1;
+    DeviceInfo dev;
+    if (device_info(&dev) != NVFP4_OK) return -1;
+    return single_token_form_of(*d, T, dev);
+}
+
+int32_t nvfp4_single_token_cluster_capacity(const moe_layer_desc* d) {
+    if (!d || check_layer(d) != NVFP4_OK) return -1;
+    DeviceInfo dev;
+    if (device_info(&dev) != NVFP4_OK) return -1;
+    return t1c_cluster_capacity(*d, dev);
+}
+
 void nvfp4_set_device_wait_limit(uint64_t limit_ns) {
     g_wait_limit.store(limit_ns == 0 ? kDefaultWaitLimit : limit_ns);
 }

@@ -16,10 +16,12 @@
 //    are requested at once, so a CTA has its whole share (or the ring's worth) of
 //    bytes in flight from the first cycle; the copies need nothing the previous
 //    kernel on the stream writes, so they are issued before griddepcontrol.wait.
-//  - Consumer warps take two rows each: with 16 warps (one token), warps 4r .. 4r+3
-//    take row pairs 0-1, 2-3, 4-5, 6-7 of the chunks c with c % 4 == r (8 warps and
-//    c % 2 when several tokens share a pass), so each activation load feeds both
-//    rows. Lane l takes the 16-byte segments l, l+32, ... of the rows (32
+//  - One token: each of the 16 consumer warps takes whole chunks (warp w the chunks
+//    c with c % 16 == w); lane l holds the activation units of segment l, l+32, ... in
+//    registers and runs them against all 8 rows, so one wait, one activation load and
+//    one 9-shuffle reduction serve 8 rows. Several tokens: 8 consumer warps, warps
+//    4r .. 4r+3 take row pairs 0-1, 2-3, 4-5, 6-7 of the chunks c with c % 2 == r, so
+//    each activation load feeds both rows. Lane l takes the 16-byte segments l, l+32, ... of the rows (32
 //    codes, two scale blocks each): cvt.rn.f16x2.e2m1x2 expands two codes
 //    into an exact f16 pair, and fma.rn.f32.f16 multiplies each code with its
 //    activation (f16) and accumulates in fp32; each 16-element partial is then
@@ -51,7 +53,11 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kCRows = 8;                              // rows per chunk (one ring slot)
-constexpr int kWarpsPerChunk = kCRows / 2;             // two rows per warp
+constexpr int kCRows1 = 8;                             // ... in the one-warp-per-chunk mode
+constexpr int kWarpsPerChunk = kCRows / 2;             // two rows per warp (several tokens)
+// consumer warps that take one chunk (GemvParams::wpc): 1 for one token when a CTA has at
+// least two chunks per consumer warp (that warp does all 8 rows, its activation segment in
+// registers across them), else 4 warps of two rows
 // consumer warps: 16 at one token (two CTAs of 17 warps fit on an SM at <= 60 registers),
 // 8 when several tokens share a pass (more accumulators per thread)
 constexpr int consumer_warps(int tc) { return tc == 1 ? 16 : 8; }
@@ -69,9 +75,11 @@ struct GemvParams {
     WsHeader* hdr;            // nullable: where a timeout is recorded
     unsigned long long wait_limit;
     int N, K, T;
-    int ngroups;              // ceil(N / 8)
+    int ngroups;              // ceil(N / crows)
+    int wpc;                  // consumer warps per chunk: 1 (one token, many chunks) or 4
     int slots;                // ring depth
-    uint32_t slot_bytes;      // kCRows * (K/2 + scale row bytes)
+    uint32_t slot_bytes;      // crows * (K/2 + scale row bytes)
+    int crows;                // rows per chunk: kCRows, or kCRows1 with one warp per chunk
     uint32_t off_ring;        // shared-memory offset of the ring (after the x stage)
 };
 
@@ -142,6 +150,65 @@ __device__ __forceinline__ void seg2(const uint32_t (&qa)[16], const uint32_t (&
     yb = fmaf(b0, pb0 + pb1, fmaf(b1, pb2 + pb3, yb));
 }
 
+// The two block scales of segment s of a scale row in shared memory (ld.shared: a select
+// between a shared and a global row would make every read a generic load).
+template <int KIND>
+__device__ __forceinline__ void seg_scales_sh(uint32_t row, int s, float& s0, float& s1) {
+    if constexpr (KIND == NVFP4_SCALE_E4M3) {
+        uint16_t b;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(row + 2u * s));
+        s0 = e4m3_to_f32(b & 0xFFu);
+        s1 = e4m3_to_f32((uint32_t)b >> 8);
+    } else if constexpr (KIND == NVFP4_SCALE_FP16) {
+        uint32_t h;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(h) : "r"(row + 4u * s));
+        s0 = f16_bits_to_f32(static_cast<uint16_t>(h & 0xFFFFu));
+        s1 = f16_bits_to_f32(static_cast<uint16_t>(h >> 16));
+    } else if constexpr (KIND == NVFP4_SCALE_FP32) {
+        float2 f;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(f.x), "=f"(f.y) : "r"(row + 8u * s));
+        s0 = f.x;
+        s1 = f.y;
+    } else {
+        uint16_t b;
+        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(b) : "r"(row + (uint32_t)s));
+        s0 = s1 = e8m0_to_f32((uint32_t)b & 0xFFu);
+    }
+}
+
+// One 16-byte segment (32 codes, two scale blocks) of one row against one token's
+// activation units (already in registers); four independent accumulators.
+__device__ __forceinline__ float seg1(const uint32_t (&q)[16], const uint4 u0, const uint4 u1, const uint4 u2,
+                                      const uint4 u3, float a0, float a1) {
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    p0 = fma2_f16(q[0], u0.x, p0);   p1 = fma2_f16(q[1], u0.y, p1);
+    p0 = fma2_f16(q[2], u0.z, p0);   p1 = fma2_f16(q[3], u0.w, p1);
+    p0 = fma2_f16(q[4], u1.x, p0);   p1 = fma2_f16(q[5], u1.y, p1);
+    p0 = fma2_f16(q[6], u1.z, p0);   p1 = fma2_f16(q[7], u1.w, p1);
+    p2 = fma2_f16(q[8], u2.x, p2);   p3 = fma2_f16(q[9], u2.y, p3);
+    p2 = fma2_f16(q[10], u2.z, p2);  p3 = fma2_f16(q[11], u2.w, p3);
+    p2 = fma2_f16(q[12], u3.x, p2);  p3 = fma2_f16(q[13], u3.y, p3);
+    p2 = fma2_f16(q[14], u3.z, p2);  p3 = fma2_f16(q[15], u3.w, p3);
+    return fmaf(a0, p0 + p1, a1 * (p2 + p3));
+}
+
+// Warp sums of v[0..7] spread over the lanes: lane l ends with the sum of v[(l >> 2) & 7]
+// (halving exchanges at distances 16, 8, 4, then the quad: 9 shuffles, a fixed order).
+__device__ __forceinline__ float warp_sum8_lanes(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w4[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 4], 16);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        w2[j] = (b3 ? w4[j + 2] : w4[j]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[j] : w4[j + 2], 8);
+    float z = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    return z;
+}
+
 __device__ __forceinline__ void expand_seg(const uint4 w, uint32_t (&q)[16]) {
     expand_word4(w.x, *reinterpret_cast<uint32_t(*)[4]>(&q[0]));
     expand_word4(w.y, *reinterpret_cast<uint32_t(*)[4]>(&q[4]));
@@ -162,7 +229,8 @@ __device__ __forceinline__ float warp_sum_pair(float a, float b, int lane) {
 template <int KIND, int TC>
 __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel(GemvParams p) {
     constexpr int kConsumerWarps = consumer_warps(TC);
-    constexpr int kChunkResidues = kConsumerWarps / kWarpsPerChunk;
+    const int wpc = TC == 1 ? p.wpc : kWarpsPerChunk;   // a constant for several tokens
+    const int kChunkResidues = kConsumerWarps / wpc;
     extern __shared__ __align__(128) uint8_t gsm[];
     __shared__ uint64_t full[kMaxSlots], empty[kMaxSlots];
     __shared__ uint32_t s_amax[kMaxTc];
@@ -176,7 +244,8 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
     const int passes = (T + TC - 1) / TC;
     const int nv = nc * passes;                    // chunks streamed by this CTA
     const uint32_t rowB = (uint32_t)K >> 1, srowB = (uint32_t)scale_row_bytes_of(KIND, K);
-    const uint32_t off_sc = kCRows * rowB;         // scale bytes inside a slot
+    const int crows = TC == 1 ? p.crows : kCRows;  // a constant for several tokens
+    const uint32_t off_sc = (uint32_t)crows * rowB;   // scale bytes inside a slot
     const int nseg = K >> 5, nunit = K >> 3;
     uint8_t* ring = gsm + p.off_ring;
     uint4* xs = reinterpret_cast<uint4*>(gsm);     // [TC][K/8] f16x8 units, interleaved
@@ -184,7 +253,7 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.slots; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarpsPerChunk);
+            mbar_init(&empty[s], TC == 1 ? p.wpc : kWarpsPerChunk);
         }
         fence_mbar_init();
     }
@@ -204,8 +273,8 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                     if (!mbar_wait_bounded(&full[slot], (uint32_t)((v / p.slots) - 1) & 1u, kDefaultWaitLimit))
                         break;
                 }
-                const int r0 = (g0 + v % nc) * kCRows;
-                const int nr = min(kCRows, N - r0);
+                const int r0 = (g0 + v % nc) * crows;
+                const int nr = min(crows, N - r0);
                 const uint32_t pb = (uint32_t)nr * rowB;                 // a multiple of 16
                 const uint32_t scb = ((uint32_t)nr * srowB) & ~15u;      // whole 16-byte units
                 uint8_t* dst = ring + (size_t)slot * p.slot_bytes;
@@ -224,8 +293,8 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
 
     // -------------------------------------------------------------------- consumers
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int res = warp / kWarpsPerChunk;          // chunk residue this warp serves
-    const int rp = 2 * (warp % kWarpsPerChunk);     // its row pair inside the chunk
+    const int res = warp / wpc;                     // chunk residue this warp serves
+    const int rp = 2 * (warp % wpc);                // its row pair inside the chunk (wpc 4)
     const int nthr = kConsumerWarps * 32;
     const float ts = __ldg(p.tscale);
     const uint16_t qnan = 0x7FC0u;
@@ -289,10 +358,60 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
 #pragma unroll
         for (int t = 0; t < TC; ++t) inv[t] = t < tc ? pow2i(-gemv_row_shift(s_amax[t])) : 0.f;
 
-        for (int ci = res; ci < nc; ci += kChunkResidues) {
+        // group `res` takes the chunks whose sequence number v = pass * nc + ci is res modulo
+        // the group count; the slot count is a multiple of it, so every slot is refilled only
+        // for the group that consumed it, which takes its fills in order (the parity of a
+        // fill's "full" phase is then never mistaken for an older one)
+        const int ci0 = ((res - (pass * nc) % kChunkResidues) % kChunkResidues + kChunkResidues) % kChunkResidues;
+        if (TC == 1 && wpc == 1) {
+            // one warp per chunk of 8 rows (each warp owns one slot): lane l takes segments l,
+            // l + 32, ... of the 8 rows with the activation segment in registers, 8 fp32 sums per
+            // lane, then one transpose reduction (warp_sum8_lanes) leaves row (l >> 2) & 7's sum
+            // on lane l
+            for (int ci = ci0; ci < nc; ci += kChunkResidues) {
+                const int v = pass * nc + ci, slot = v % p.slots;
+                if (ok && !mbar_wait_bounded(&full[slot], (uint32_t)(v / p.slots) & 1u, p.wait_limit)) ok = false;
+                const int r0 = (g0 + ci) * kCRows1, nr = min(kCRows1, N - r0);
+                if (!ok) {
+                    if (lane < nr) p.y[r0 + lane] = qnan;
+                } else {
+                    const uint8_t* slotp = ring + (size_t)slot * p.slot_bytes;
+                    const uint32_t slot_sa = smem_addr(slotp);
+                    const uint32_t scb = ((uint32_t)nr * srowB) & ~15u;
+                    float acc[kCRows1];
+#pragma unroll
+                    for (int rr = 0; rr < kCRows1; ++rr) acc[rr] = 0.f;
+                    for (int s = lane; s < nseg; s += 32) {
+                        const uint4 u0 = xs[s], u1 = xs[nseg + s], u2 = xs[2 * nseg + s], u3 = xs[3 * nseg + s];
+#pragma unroll
+                        for (int rr = 0; rr < kCRows1; ++rr) {
+                            if (rr < nr) {
+                                // a row whose scales did not fit the chunk's whole 16-byte units
+                                // (only in a ragged last chunk) reads them from global memory
+                                float a0, a1;
+                                if ((uint32_t)(rr + 1) * srowB <= scb)
+                                    seg_scales_sh<KIND>(slot_sa + off_sc + (uint32_t)rr * srowB, s, a0, a1);
+                                else
+                                    seg_scales<KIND>(p.scales + (size_t)(r0 + rr) * srowB, s, a0, a1);
+                                uint32_t q[16];
+                                expand_seg(reinterpret_cast<const uint4*>(slotp + (size_t)rr * rowB)[s], q);
+                                acc[rr] += seg1(q, u0, u1, u2, u3, a0, a1);
+                            }
+                        }
+                    }
+                    const float z = warp_sum8_lanes(acc, lane);
+                    const int rr = (lane >> 2) & 7;
+                    if ((lane & 3) == 0 && rr < nr) p.y[r0 + rr] = f32_to_bf16((z * ts) * inv[0]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            continue;
+        }
+        for (int ci = ci0; ci < nc; ci += kChunkResidues) {
             const int v = pass * nc + ci, slot = v % p.slots;
             if (ok && !mbar_wait_bounded(&full[slot], (uint32_t)(v / p.slots) & 1u, p.wait_limit)) ok = false;
-            const int r0 = (g0 + ci) * kCRows, ra = r0 + rp;
+            const int r0 = (g0 + ci) * crows, ra = r0 + rp;
             if (ra < N) {
                 const bool has_b = ra + 1 < N;
                 if (!ok) {
@@ -304,17 +423,17 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                     const uint8_t* slotp = ring + (size_t)slot * p.slot_bytes;
                     const uint8_t* rowa = slotp + (size_t)rp * rowB;
                     const uint8_t* rowb = has_b ? rowa + rowB : rowa;
-                    const int nr = min(kCRows, N - r0);
+                    const int nr = min(crows, N - r0);
                     const uint32_t scb = ((uint32_t)nr * srowB) & ~15u;
                     // a row whose scales did not fit the chunk's whole 16-byte units (only in a
                     // ragged last chunk) reads them from global memory
-                    const uint8_t* sra = ((uint32_t)(rp + 1) * srowB <= scb)
-                                             ? slotp + off_sc + (size_t)rp * srowB
-                                             : p.scales + (size_t)ra * srowB;
                     const int rb = has_b ? ra + 1 : ra;
-                    const uint8_t* srb = ((uint32_t)(rp + (has_b ? 2 : 1)) * srowB <= scb)
-                                             ? slotp + off_sc + (size_t)(rb - r0) * srowB
-                                             : p.scales + (size_t)rb * srowB;
+                    const bool sa_sh = (uint32_t)(rp + 1) * srowB <= scb;
+                    const bool sb_sh = (uint32_t)(rp + (has_b ? 2 : 1)) * srowB <= scb;
+                    const uint32_t sra_sh = smem_addr(slotp) + off_sc + (uint32_t)rp * srowB;
+                    const uint32_t srb_sh = smem_addr(slotp) + off_sc + (uint32_t)(rb - r0) * srowB;
+                    const uint8_t* sra = p.scales + (size_t)ra * srowB;
+                    const uint8_t* srb = p.scales + (size_t)rb * srowB;
                     float acca[TC], accb[TC];
 #pragma unroll
                     for (int t = 0; t < TC; ++t) acca[t] = accb[t] = 0.f;
@@ -323,8 +442,10 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                         const uint4 wa = reinterpret_cast<const uint4*>(rowa)[s];
                         const uint4 wb = reinterpret_cast<const uint4*>(rowb)[s];
                         float a0, a1, b0, b1;
-                        seg_scales<KIND>(sra, s, a0, a1);
-                        seg_scales<KIND>(srb, s, b0, b1);
+                        if (sa_sh) seg_scales_sh<KIND>(sra_sh, s, a0, a1);
+                        else seg_scales<KIND>(sra, s, a0, a1);
+                        if (sb_sh) seg_scales_sh<KIND>(srb_sh, s, b0, b1);
+                        else seg_scales<KIND>(srb, s, b0, b1);
                         uint32_t qa[16], qb[16];
                         expand_seg(wa, qa);
                         expand_seg(wb, qb);
@@ -351,7 +472,7 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
 }
 
 struct GemvPlan {
-    int tc, slots, grid;
+    int tc, slots, grid, wpc, crows;
     uint32_t slot_bytes, off_ring, smem;
 };
 
@@ -362,22 +483,46 @@ GemvPlan plan_gemv(const nvfp4_weight& W, int T, const DeviceInfo& dev) {
     g.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
     if (T == 3) g.tc = 4;
     if (T >= 5 && T < 8) g.tc = 8;
+    g.off_ring = (uint32_t)g.tc * (uint32_t)K * 2u;
+    const int passes = (T + g.tc - 1) / g.tc;
+    // one token with at least two chunks per consumer warp: one warp per chunk, each of the
+    // 16 warps owning one ring slot (one CTA per SM)
+    {
+        const int cw1 = consumer_warps(1);
+        const int ng1 = (N + kCRows1 - 1) / kCRows1;
+        const int grid1 = ng1 < dev.num_sms ? ng1 : dev.num_sms;
+        const uint32_t sb1 = (uint32_t)kCRows1 * ((uint32_t)K / 2 + srow);
+        if (g.tc == 1 && (ng1 + grid1 - 1) / grid1 >= 2 * cw1 &&
+            g.off_ring + (uint32_t)cw1 * sb1 + 2048u <= (uint32_t)dev.smem_optin) {
+            g.wpc = 1;
+            g.crows = kCRows1;
+            g.grid = grid1;
+            g.slot_bytes = sb1;
+            g.slots = cw1;
+            g.smem = g.off_ring + (uint32_t)g.slots * g.slot_bytes;
+            return g;
+        }
+    }
+    g.wpc = kWarpsPerChunk;
+    g.crows = kCRows;
     const int ngroups = (N + kCRows - 1) / kCRows;
     g.grid = ngroups < dev.num_sms ? ngroups : dev.num_sms;
     const int nc_max = (ngroups + g.grid - 1) / g.grid;
-    const int passes = (T + g.tc - 1) / g.tc;
     g.slot_bytes = (uint32_t)kCRows * ((uint32_t)K / 2 + srow);
-    g.off_ring = (uint32_t)g.tc * (uint32_t)K * 2u;
+    const long want = (long)nc_max * passes;
     // two CTAs per SM when the ring and stage fit in ~100 KB (the next launch's
     // weight prologue then overlaps this one under programmatic dependent launch)
     const uint32_t small_cap = 100u * 1024u;
     const uint32_t cap = (g.off_ring + 2u * g.slot_bytes <= small_cap) ? small_cap
                                                                        : (uint32_t)dev.smem_optin - 2048u;
-    long slots = ((long)cap - (long)g.off_ring) / (long)g.slot_bytes;
-    const long want = (long)nc_max * passes;
-    if (slots > want) slots = want;
-    if (slots > kMaxSlots) slots = kMaxSlots;
-    if (slots < 1) slots = 1;
+    long fit = ((long)cap - (long)g.off_ring) / (long)g.slot_bytes;
+    if (fit > kMaxSlots) fit = kMaxSlots;
+    // a multiple of the consumer groups (each group owns the slots of its residue): the
+    // chunk count rounded up where that fits, else the largest multiple that fits
+    const int groups = consumer_warps(g.tc) / kWarpsPerChunk;
+    long slots = (want + groups - 1) / groups * groups;
+    if (slots > fit) slots = fit / groups * groups;
+    if (slots < groups) slots = groups;
     g.slots = (int)slots;
     g.smem = g.off_ring + (uint32_t)g.slots * g.slot_bytes;
     return g;
@@ -433,7 +578,9 @@ cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_
     P.N = W.N;
     P.K = W.K;
     P.T = T;
-    P.ngroups = (W.N + kCRows - 1) / kCRows;
+    P.ngroups = (W.N + g.crows - 1) / g.crows;
+    P.wpc = g.wpc;
+    P.crows = g.crows;
     P.slots = g.slots;
     P.slot_bytes = g.slot_bytes;
     P.off_ring = g.off_ring;

@@ -33,8 +33,16 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
 constexpr int kWordReplicas = 8;
 __host__ __device__ inline size_t t1_logit_stride(const moe_layer_desc& d) { return ((size_t)d.E + 1 + 15) & ~size_t(15); }
 __host__ __device__ inline size_t t1_h_stride(const moe_layer_desc& d) { return ((size_t)d.k * d.I + d.Is + 31) & ~size_t(31); }
+// Exchange area of the cluster form, in 8-byte units: kWordReplicas copies of the Is shared
+// values (4-byte tagged words, each copy padded to 32 words), then k * H tagged partial
+// outputs (8-byte words).
+__host__ __device__ inline size_t t1c_words(const moe_layer_desc& d) {
+    return (size_t)kWordReplicas * ((((size_t)d.Is + 31) & ~size_t(31)) / 2) + (size_t)d.k * d.H;
+}
 __host__ __device__ inline size_t t1_words(const moe_layer_desc& d) {
-    return (size_t)kWordReplicas * (t1_logit_stride(d) + t1_h_stride(d) / 2);
+    const size_t grid = (size_t)kWordReplicas * (t1_logit_stride(d) + t1_h_stride(d) / 2);
+    const size_t cl = t1c_words(d);
+    return grid > cl ? grid : cl;
 }
 
 // Workspace of one layer call (device scratch carved from the caller's buffer).
@@ -71,8 +79,25 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
                                   int32_t* ids_out, float* w_out, const LayerWs& ws, const DeviceInfo& dev,
                                   cudaStream_t s, const uint16_t* resid = nullptr);
 
-// One-launch single-token decode (persistent grid, two bounded grid barriers).
+// Launch tags of the single-token kernels: every launch adds tag_period(dev) to the
+// workspace counter (each of its CTAs adds tag_period / grid size), so the counter is a
+// multiple of the period between launches of either form, and a launch's tag is
+// counter / period + 1 at any of its CTAs.
+unsigned long long t1_tag_period(const DeviceInfo& dev);
+
+// Single-token decode in one launch: the persistent-grid form, or on request the cluster
+// form (k clusters of 8 to 16 CTAs) where the shape and the device allow it. form: 0 =
+// automatic (the grid form), 1 = grid form, 2 = cluster form (unsupported -> grid form).
+void set_t1_form(int form);
+bool t1c_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev);
+cudaError_t launch_moe_decode_t1c(const moe_layer_desc& d, const uint16_t* x, uint16_t* y, int32_t* ids_out,
+                                  float* w_out, const LayerWs& ws, const DeviceInfo& dev, uint64_t wait_limit,
+                                  cudaStream_t s, const uint16_t* norm_w, float eps, const uint16_t* resid);
 bool fused_decode_supported(const moe_layer_desc& d, int T, const DeviceInfo& dev);
+// 2: the cluster form runs this call, 1: the grid form, 0: neither (T != 1 or the shape)
+int single_token_form_of(const moe_layer_desc& d, int T, const DeviceInfo& dev);
+// resident 16-CTA clusters of the cluster form for this layer (0 when the shape has none)
+int t1c_cluster_capacity(const moe_layer_desc& d, const DeviceInfo& dev);
 cudaError_t launch_moe_decode_fused(const moe_layer_desc& d, const uint16_t* x, uint16_t* y,
                                     int32_t* ids_out, float* w_out, const LayerWs& ws,
                                     const DeviceInfo& dev, uint64_t wait_limit, cudaStream_t s,

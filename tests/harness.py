@@ -233,3 +233,19 @@ class ParityCheck:
             ok2, err2, bound2 = tol_ok(self.y, ref, rel=self.rel_only, abs_=0.0)
             assert ok2, "max|gpu-oracle| %.4g > %.4g (scale-free)" % (err2, bound2)
         return err, bound, int(self.near.size)
+
+
+class single_token_form:
+    """Run the enclosed calls with the given single-token kernel form (1 the persistent-grid
+    form, 2 the cluster form where supported), then restore automatic (the grid form)."""
+
+    def __init__(self, nv, form: int):
+        self.nv, self.form = nv, form
+
+    def __enter__(self):
+        self.nv.set_single_token_form(self.form)
+        return self
+
+    def __exit__(self, *exc):
+        self.nv.set_single_token_form(0)
+        return False

@@ -11,7 +11,8 @@ import torch
 
 import oracle
 import workload as wl
-from harness import ParityCheck, check_layer_parity, gpu_layer, margin_tokens, oracle_layer, tol_ok
+from harness import (ParityCheck, check_layer_parity, gpu_layer, margin_tokens, oracle_layer, single_token_form,
+                     tol_ok)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,15 +42,18 @@ def test_tiny_layer_tokens(nv, T):
     check_layer_parity(L, x, y, ids, w)
 
 
-def test_decode_one_token_seeds_0_31(nv):
+@pytest.mark.parametrize("form", [2, 1], ids=["cluster", "grid"])
+def test_decode_one_token_seeds_0_31(nv, form):
     """Single-token decode through a Qwen3.6-35B-A3B-shaped layer, seeds 0..31,
-    router margins above 1e-3 (tokens redrawn from their seed stream until so)."""
+    router margins above 1e-3 (tokens redrawn from their seed stream until so), on the
+    cluster form and on the persistent-grid form."""
     errs = []
     for seed in range(32):
         L = wl.LayerInputs(QW, seed=seed)
         layer = gpu_layer(L)
         x, _ = margin_tokens(L, seed, 1)
-        y, ids, w = _forward(nv, layer, x)
+        with single_token_form(nv, form):
+            y, ids, w = _forward(nv, layer, x)
         err, bound, near = check_layer_parity(L, x, y, ids, w)
         assert near == 0
         errs.append(err / bound)

@@ -77,6 +77,19 @@ def test_residual_layer(nv, shape, T):
     _check(L, h, w, out, ids)
 
 
+def test_residual_layer_grid_form(nv):
+    """The fused single-token norm + residual on the persistent-grid form as well."""
+    from harness import single_token_form
+    shape = wl.QWEN36_35B_A3B
+    L = wl.LayerInputs(shape, seed=21)
+    layer = gpu_layer(L)
+    h, w = _inputs(shape, 21, 1)
+    with single_token_form(nv, 1):
+        out, ids, _ = nv.moe_layer_forward_residual(layer, h.cuda(), w.cuda(), EPS, want_route=True)
+        torch.cuda.synchronize()
+    _check(L, h, w, out, ids)
+
+
 def test_residual_layer_fp16_scales(nv):
     shape = wl.MoEShape(H=512, E=32, k=4, I=256, Is=128)
     L = wl.LayerInputs(shape, seed=23)

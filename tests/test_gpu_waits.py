@@ -8,27 +8,72 @@ import pytest
 import torch
 
 import workload as wl
-from harness import check_layer_parity, gpu_layer
+from harness import check_layer_parity, gpu_layer, single_token_form
 
 pytestmark = pytest.mark.gpu
 
 
-def test_grid_barrier_timeout_is_reported(nv):
+def _tag_period(sms):
+    # every single-token launch adds this to the workspace's launch counter (the lcm of the
+    # grid sizes either form can launch: the SM count and cs * k, cs in {8, 12, 16}, k <= 8)
+    from math import gcd
+    l = sms
+    for cs in (8, 12, 16):
+        for k in range(1, 9):
+            l = l // gcd(l, cs * k) * (cs * k)
+    return l
+
+
+@pytest.mark.parametrize("form", [2, 1], ids=["cluster", "grid"])
+def test_split_launch_tags_time_out(nv, form):
+    """The host drops the counter one short of a launch boundary, so the first CTA of the
+    next launch takes one tag and the others the next: their exchange words never match,
+    every bounded poll runs out (a flag that nothing sets), the timeout is recorded and the
+    CTAs return; after re-initialising the workspace the same call is correct."""
+    L = wl.LayerInputs(wl.SMALL256, seed=2)
+    layer = gpu_layer(L)
+    x = wl.activations(2, 1, 256).cuda()
+    ws = nv.Workspace(nv.moe_layer_workspace_size(layer, 1))
+    with single_token_form(nv, form):
+        assert nv.single_token_form_used(layer, 1) in ((2, 1) if form == 2 else (1,))
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        start = torch.tensor([_tag_period(sms) - 1], dtype=torch.int64, device="cuda")
+        ws.buf[8:16].copy_(start.view(torch.uint8))      # the header's launch counter
+        try:
+            nv.set_device_wait_limit(1_000_000)           # 1 ms
+            nv.moe_layer_forward(layer, x, ws=ws)
+            torch.cuda.synchronize()
+            assert ws.status(clear=True) == nv.NVFP4_ERR_DEVICE_TIMEOUT
+        finally:
+            nv.set_device_wait_limit(0)
+        nv.lib.nvfp4_workspace_init(ws.ptr(), ws.nbytes, nv._stream())
+        y, ids, w = nv.moe_layer_forward(layer, x, ws=ws, want_route=True)
+        torch.cuda.synchronize()
+        assert ws.status() == nv.NVFP4_OK
+        check_layer_parity(L, x, y, ids, w)
+
+
+@pytest.mark.parametrize("form", [2, 1], ids=["cluster", "grid"])
+def test_grid_barrier_timeout_is_reported(nv, form):
     L = wl.LayerInputs(wl.SMALL256, seed=0)
     layer = gpu_layer(L)
     x = wl.activations(0, 1, 256).cuda()
     ws = nv.Workspace(nv.moe_layer_workspace_size(layer, 1))
-    try:
-        nv.set_device_wait_limit(1)
-        nv.moe_layer_forward(layer, x, ws=ws)
+    with single_token_form(nv, form):
+        try:
+            nv.set_device_wait_limit(1)
+            nv.moe_layer_forward(layer, x, ws=ws)
+            torch.cuda.synchronize()
+            st = ws.status(clear=True)
+            # the grid form always polls before its peers publish; the cluster form's few
+            # global polls can find their words already there (then the call is complete)
+            assert st == nv.NVFP4_ERR_DEVICE_TIMEOUT or (form == 2 and st == nv.NVFP4_OK)
+        finally:
+            nv.set_device_wait_limit(0)
+        # the context is still usable; a fresh workspace state gives the right answer
+        nv.lib.nvfp4_workspace_init(ws.ptr(), ws.nbytes, nv._stream())
+        y, ids, w = nv.moe_layer_forward(layer, x, ws=ws, want_route=True)
         torch.cuda.synchronize()
-        assert ws.status(clear=True) == nv.NVFP4_ERR_DEVICE_TIMEOUT
-    finally:
-        nv.set_device_wait_limit(0)
-    # the context is still usable; a fresh workspace state gives the right answer
-    nv.lib.nvfp4_workspace_init(ws.ptr(), ws.nbytes, nv._stream())
-    y, ids, w = nv.moe_layer_forward(layer, x, ws=ws, want_route=True)
-    torch.cuda.synchronize()
     assert ws.status() == nv.NVFP4_OK
     check_layer_parity(L, x, y, ids, w)
 
