@@ -42,10 +42,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--seeds", type=int, default=N_SEEDS, help="layer instances to rotate over")
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched", "gemv"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "batched", "gemv", "lm_head"],
                     help="decode: the single-token layer (default, the headline); prefill: one "
                          "4096-token layer call with the skewed router; batched: one --tokens-token "
-                         "decode call per step; gemv: the dense W4A16 GEMV, 1 token, K=2048 -> N=8192")
+                         "decode call per step; gemv: the dense W4A16 GEMV, 1 token, K=2048 -> N=8192 "
+                         "(and the lm_head); lm_head: the 248320 x 2048 lm_head GEMV alone")
     ap.add_argument("--tokens", type=int, default=64, help="tokens per call of --workload batched (1..64)")
     ap.add_argument("--no-extras", action="store_true",
                     help="default workload: time only the single-token steps (skip the batched, 40-layer, "
@@ -501,9 +502,17 @@ def measure_gemv(nv, wl, device, reps=10):
         if clk:
             res["clocks"] = clk
         del Ws, xs, ys, g
-    # the lm_head of the same model: vocab 248320 x hidden 2048 (318 / 287 MB per call, two
-    # instances rotating, each larger than L2)
-    N, n_inst = 248320, 2
+    res.update(measure_lm_head(nv, wl, device, reps))
+    res["peak_kind"] = peak_kind
+    return res
+
+
+def measure_lm_head(nv, wl, device, reps=10):
+    """The lm_head of the same model as one dense GEMV: vocab 248320 x hidden 2048 (318 / 287
+    MB per call with FP16 / E4M3 block scales), two instances rotating, each larger than L2."""
+    N, K, T, n_inst = 248320, 2048, 1, 2
+    stream = torch.cuda.current_stream()
+    res = {}
     for kind, name in ((nv.SCALE_FP16, "lm_head_fp16"), (nv.SCALE_E4M3, "lm_head_e4m3")):
         Ws = []
         for i in range(n_inst):
@@ -522,12 +531,12 @@ def measure_gemv(nv, wl, device, reps=10):
         ms, _ = time_graph(g, r2, stream, device)
         us = 1e3 * ms / (r2 * n_inst)
         gbs = bytes_call / (us * 1e-6) / 1e9
+        peak, _ = measured_peaks()
         res[name] = {"us_per_call": us, "bytes_per_call": bytes_call, "achieved_gbs": gbs,
                      "frac_of_hbm_peak": gbs / peak if peak else None, "calls": r2 * n_inst,
                      "shape": "T=1, K=2048 -> N=248320"}
         del Ws, xs, ys, g
         torch.cuda.empty_cache()
-    res["peak_kind"] = peak_kind
     return res
 
 
@@ -551,6 +560,31 @@ def run_gemv(args, nv, wl, device):
         "e4m3": res["e4m3"],
         "gpu_launches": f["calls"],
         "clocks": res.get("clocks"),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_lm_head(args, nv, wl, device):
+    reps = max(4, -(-max(1, args.steps) // 2))
+    res = measure_lm_head(nv, wl, device, reps)
+    f = res["lm_head_fp16"]
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": "NVFP4 lm_head GEMV, 1 token, K=2048 -> N=248320: us per call and achieved HBM GB/s",
+        "value": f["us_per_call"], "unit": "us/call", "n_gpus": 1, "steps": f["calls"], "warmup": 3,
+        "ms_per_step": f["us_per_call"] * 1e-3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16-act/nvfp4-weight, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights packed to NVFP4, x ~ N(0,1) bf16)",
+        "config": {"workload": "NVFP4 lm_head GEMV (vocabulary 248320 x hidden 2048), T=1, FP16 per-16 scales; "
+                               "2 rotating weight instances (318 MB each)", "tokens_per_step": 1,
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": f["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": f["frac_of_hbm_peak"], "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": f["bytes_per_call"], "kernel": "gemv_kernel (one launch per call)"},
+        "e4m3": res["lm_head_e4m3"],
+        "gpu_launches": f["calls"],
         "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
@@ -584,6 +618,10 @@ def main():
         if world > 1 and rank != 0:
             return 0
         return run_gemv(args, nv, wl, device)
+    if args.workload == "lm_head":
+        if world > 1 and rank != 0:
+            return 0
+        return run_lm_head(args, nv, wl, device)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
