@@ -264,6 +264,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return true;
 }
 
+// Bounded wait that ignores the abort flag: after an abort, a thread that issued bulk copies
+// or MMAs waits (with the library's fixed limit) until they have landed, so that the CTA
+// never exits with its own asynchronous operations in flight.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    mbar_wait_bounded(bar, parity, kDefaultWaitLimit);
+}
+
 constexpr int kHS = kM + 8;   // bf16 staging row stride of the gate/up epilogue
 constexpr int kYS = kM + 4;   // fp32 staging row stride of the down epilogue
 
@@ -397,17 +404,22 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
                 y0 = (shared ? 0 : tr.slot * P.H) + feat0;
                 y1 = y0 + kM;
             }
+            int issued = 0;
 #pragma unroll 1
             for (int s = 0; s < nk; ++s) {
                 const int r = s % R, u = s / R;
-                if (u > 0) wait_or_abort(&raw_empty[r], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                if (u > 0 && !wait_or_abort(&raw_empty[r], (u - 1) & 1, abort_flag, hdr, wait_limit)) break;
+                if (*abort_flag) break;
                 const uint32_t raw = sm_base + offRaw + r * kRawStage;
                 mbar_arrive_expect_tx(&raw_full[r], 2 * (32 * kM) + 2 * (16 * kM));
                 tma_load_2d(raw, mc, s * 32, y0, &raw_full[r]);
                 tma_load_2d(raw + kM * 32, mc, s * 32, y1, &raw_full[r]);
                 tma_load_2d(raw + kRawScales, ms, (s >> 2) * 16, y0, &raw_full[r]);
                 tma_load_2d(raw + kRawScales + kM * 16, ms, (s >> 2) * 16, y1, &raw_full[r]);
+                issued = s + 1;
             }
+            // every issued copy has landed before the CTA may exit (the last fill of each slot)
+            for (int s = max(0, issued - R); s < issued; ++s) drain_wait(&raw_full[s % R], (s / R) & 1);
         }
     } else if (warp >= kBWarp0 && warp < kMmaWarp) {
         // ---------------- token-row stream, up to SB steps ahead of the MMAs (gate/up:
@@ -425,7 +437,8 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
 #pragma unroll 1
             for (int s = 0; s < nk; ++s) {
                 const int b = s % SB, u = s / SB;
-                if (u > 0) wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                if (u > 0 && !wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit)) break;
+                if (*abort_flag) break;
                 const uint32_t bb = sm_base + offB + b * bbytes;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -438,17 +451,22 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
                 }
                 cp_async_arrive_noinc(&b_full[b]);
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's copies have landed
         } else if (bt == 0) {
             const CUtensorMap* mb = shared ? &maps.hs : &maps.h;
+            int issued = 0;
 #pragma unroll 1
             for (int s = 0; s < nk; ++s) {
                 const int b = s % SB, u = s / SB;
-                if (u > 0) wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit);
+                if (u > 0 && !wait_or_abort(&b_empty[b], (u - 1) & 1, abort_flag, hdr, wait_limit)) break;
+                if (*abort_flag) break;
                 const uint32_t bb = sm_base + offB + b * bbytes;
                 mbar_arrive_expect_tx(&b_full[b], (uint32_t)bbytes);
                 for (int i = 0; i < N / kBoxRowsB; ++i)
                     tma_load_2d(bb + i * (kBoxRowsB * 128), mb, s * kKS, tr.p0 + i * kBoxRowsB, &b_full[b]);
+                issued = s + 1;
             }
+            for (int s = max(0, issued - SB); s < issued; ++s) drain_wait(&b_full[s % SB], (s / SB) & 1);
         }
     } else if (warp < kExp / 32) {
         // ---------------- expanders: raw NVFP4 bytes -> bf16 A tile (half a row each)
@@ -493,7 +511,10 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
         }
 
         // ---------------- epilogue: TMEM -> registers -> shared staging -> global
-        wait_or_abort(accb, 0, abort_flag, hdr, wait_limit);
+        // (after an abort: still wait, with the fixed limit, until the MMAs the issuer committed
+        // are done, so that no read of tensor memory races them; the outputs are then garbage
+        // and the call reports the timeout)
+        if (!wait_or_abort(accb, 0, abort_flag, hdr, wait_limit)) drain_wait(accb, 0);
         tc_fence_after();
         const int q = warp & 3, c_begin = (warp >> 2) * (kTokTile / 4);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
@@ -577,6 +598,9 @@ grouped_tc_kernel(const GroupedParams P, const __grid_constant__ TcMaps maps, in
             tc_commit(&b_empty[b]);
         }
         tc_commit(accb);
+        // after an abort the epilogue does not wait for the MMAs: wait here (fixed limit) so that
+        // none is still writing tensor memory when it is freed
+        if (*abort_flag) drain_wait(accb, 0);
     }
     tc_fence_before();
     __syncthreads();

@@ -138,3 +138,26 @@ def test_qwen_prefill_4096_zipf(nv):
     g = np.bincount(ids.cpu().numpy().ravel(), minlength=shape.E)
     assert abs(int(g.max()) - gold["max_count"]) <= 8
     ParityCheck(L, x, y, ids, w).check()
+
+
+def test_prefill_wait_timeout_is_reported(nv):
+    """The grouped tensor-core kernels' bounded waits with the limit at 1 ns: the first wait
+    that is not already satisfied runs out, the CTA raises its abort flag, stops issuing copies
+    and MMAs, waits (with the library's fixed limit) for the ones in flight, frees its tensor
+    memory and returns; the workspace records the timeout. Afterwards the same call is correct."""
+    L = wl.LayerInputs(wl.SMALL256, seed=31)
+    layer = gpu_layer(L)
+    x = wl.activations(31, 300, 256)
+    ws = nv.Workspace(nv.moe_layer_workspace_size(layer, 300))
+    try:
+        nv.set_device_wait_limit(1)
+        nv.moe_layer_forward(layer, x.cuda(), ws=ws)
+        torch.cuda.synchronize()
+        assert ws.status(clear=True) == nv.NVFP4_ERR_DEVICE_TIMEOUT
+    finally:
+        nv.set_device_wait_limit(0)
+    nv.lib.nvfp4_workspace_init(ws.ptr(), ws.nbytes, nv._stream())
+    y, ids, w = nv.moe_layer_forward(layer, x.cuda(), ws=ws, want_route=True)
+    torch.cuda.synchronize()
+    assert ws.status() == nv.NVFP4_OK
+    check_layer_parity(L, x, y, ids, w)
