@@ -7,8 +7,8 @@
 // The weight stream is what bounds this call (4.5 bits per weight against 16 bits
 // of activation per token), so the kernel is built around keeping HBM busy:
 //
-//  - A persistent grid of one CTA per SM. The rows are cut into groups of 8 and
-//    CTA c owns the contiguous groups [ng*c/G, ng*(c+1)/G): every CTA streams one
+//  - A persistent grid of one CTA per SM. The rows are cut into chunks (8 or 32 rows)
+//    and CTA c owns the contiguous chunks [ng*c/G, ng*(c+1)/G): every CTA streams one
 //    contiguous byte range of the packed codes and one of the block scales.
 //  - One producer warp moves each 8-row chunk HBM -> shared memory with two TMA
 //    bulk copies (codes, scales) into a ring of slots, each with a "full" mbarrier
@@ -16,12 +16,15 @@
 //    are requested at once, so a CTA has its whole share (or the ring's worth) of
 //    bytes in flight from the first cycle; the copies need nothing the previous
 //    kernel on the stream writes, so they are issued before griddepcontrol.wait.
-//  - One token: each of the 16 consumer warps takes whole chunks (warp w the chunks
-//    c with c % 16 == w); lane l holds the activation units of segment l, l+32, ... in
-//    registers and runs them against all 8 rows, so one wait, one activation load and
-//    one 9-shuffle reduction serve 8 rows. Several tokens: 8 consumer warps, warps
-//    4r .. 4r+3 take row pairs 0-1, 2-3, 4-5, 6-7 of the chunks c with c % 2 == r, so
-//    each activation load feeds both rows. Lane l takes the 16-byte segments l, l+32, ... of the rows (32
+//  - One token and a long row range per CTA (the lm_head): chunks of 32 rows (each SM
+//    keeps only a few bulk copies in flight, so the copies are made large: 32 rows cut
+//    the lm_head from 97.5 to 75.2 us against 8-row chunks), 4 warps per chunk with 8 rows
+//    each; lane l holds the activation units of segments l, l+32, ... in registers and
+//    runs them against its warp's 8 rows, so one wait, one activation load and one
+//    9-shuffle reduction serve 8 rows. Otherwise chunks of 8 rows: one token with few
+//    chunks per CTA, 16 consumer warps, warps 4r .. 4r+3 take row pairs 0-1, 2-3, 4-5,
+//    6-7 of the chunks of group r; several tokens, 8 consumer warps and 2 groups; each
+//    activation load feeds both rows. Lane l takes the 16-byte segments l, l+32, ... of the rows (32
 //    codes, two scale blocks each): cvt.rn.f16x2.e2m1x2 expands two codes
 //    into an exact f16 pair, and fma.rn.f32.f16 multiplies each code with its
 //    activation (f16) and accumulates in fp32; each 16-element partial is then
@@ -76,7 +79,9 @@ struct GemvParams {
     unsigned long long wait_limit;
     int N, K, T;
     int ngroups;              // ceil(N / crows)
-    int wpc;                  // consumer warps per chunk: 1 (one token, many chunks) or 4
+    int wpc;                  // consumer warps per chunk
+    int wide;                 // 1: one token, each warp takes 8 rows of a chunk of 8 * wpc rows
+                              // (big copies); 0: chunks of 8 rows, two rows per warp
     int slots;                // ring depth
     uint32_t slot_bytes;      // crows * (K/2 + scale row bytes)
     int crows;                // rows per chunk: kCRows, or kCRows1 with one warp per chunk
@@ -230,6 +235,7 @@ template <int KIND, int TC>
 __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel(GemvParams p) {
     constexpr int kConsumerWarps = consumer_warps(TC);
     const int wpc = TC == 1 ? p.wpc : kWarpsPerChunk;   // a constant for several tokens
+    const bool wide = TC == 1 && p.wide;
     const int kChunkResidues = kConsumerWarps / wpc;
     extern __shared__ __align__(128) uint8_t gsm[];
     __shared__ uint64_t full[kMaxSlots], empty[kMaxSlots];
@@ -363,21 +369,25 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
         // for the group that consumed it, which takes its fills in order (the parity of a
         // fill's "full" phase is then never mistaken for an older one)
         const int ci0 = ((res - (pass * nc) % kChunkResidues) % kChunkResidues + kChunkResidues) % kChunkResidues;
-        if (TC == 1 && wpc == 1) {
+        if (wide) {
             // one warp per chunk of 8 rows (each warp owns one slot): lane l takes segments l,
             // l + 32, ... of the 8 rows with the activation segment in registers, 8 fp32 sums per
             // lane, then one transpose reduction (warp_sum8_lanes) leaves row (l >> 2) & 7's sum
             // on lane l
+            const int rb8 = 8 * (warp % wpc);            // this warp's 8 rows inside the chunk
             for (int ci = ci0; ci < nc; ci += kChunkResidues) {
                 const int v = pass * nc + ci, slot = v % p.slots;
                 if (ok && !mbar_wait_bounded(&full[slot], (uint32_t)(v / p.slots) & 1u, p.wait_limit)) ok = false;
-                const int r0 = (g0 + ci) * kCRows1, nr = min(kCRows1, N - r0);
-                if (!ok) {
+                const int c0r = (g0 + ci) * crows;                    // the chunk's first row
+                const int nrc = min(crows, N - c0r);                  // rows in the chunk
+                const int r0 = c0r + rb8, nr = min(kCRows1, nrc - rb8);   // this warp's rows
+                if (nr <= 0) {
+                } else if (!ok) {
                     if (lane < nr) p.y[r0 + lane] = qnan;
                 } else {
                     const uint8_t* slotp = ring + (size_t)slot * p.slot_bytes;
                     const uint32_t slot_sa = smem_addr(slotp);
-                    const uint32_t scb = ((uint32_t)nr * srowB) & ~15u;
+                    const uint32_t scb = ((uint32_t)nrc * srowB) & ~15u;
                     float acc[kCRows1];
 #pragma unroll
                     for (int rr = 0; rr < kCRows1; ++rr) acc[rr] = 0.f;
@@ -389,12 +399,12 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
                                 // a row whose scales did not fit the chunk's whole 16-byte units
                                 // (only in a ragged last chunk) reads them from global memory
                                 float a0, a1;
-                                if ((uint32_t)(rr + 1) * srowB <= scb)
-                                    seg_scales_sh<KIND>(slot_sa + off_sc + (uint32_t)rr * srowB, s, a0, a1);
+                                if ((uint32_t)(rb8 + rr + 1) * srowB <= scb)
+                                    seg_scales_sh<KIND>(slot_sa + off_sc + (uint32_t)(rb8 + rr) * srowB, s, a0, a1);
                                 else
                                     seg_scales<KIND>(p.scales + (size_t)(r0 + rr) * srowB, s, a0, a1);
                                 uint32_t q[16];
-                                expand_seg(reinterpret_cast<const uint4*>(slotp + (size_t)rr * rowB)[s], q);
+                                expand_seg(reinterpret_cast<const uint4*>(slotp + (size_t)(rb8 + rr) * rowB)[s], q);
                                 acc[rr] += seg1(q, u0, u1, u2, u3, a0, a1);
                             }
                         }
@@ -472,7 +482,7 @@ __global__ void __launch_bounds__(gemv_threads(TC), TC <= 2 ? 2 : 1) gemv_kernel
 }
 
 struct GemvPlan {
-    int tc, slots, grid, wpc, crows;
+    int tc, slots, grid, wpc, crows, wide;
     uint32_t slot_bytes, off_ring, smem;
 };
 
@@ -485,24 +495,28 @@ GemvPlan plan_gemv(const nvfp4_weight& W, int T, const DeviceInfo& dev) {
     if (T >= 5 && T < 8) g.tc = 8;
     g.off_ring = (uint32_t)g.tc * (uint32_t)K * 2u;
     const int passes = (T + g.tc - 1) / g.tc;
-    // one token with at least two chunks per consumer warp: one warp per chunk, each of the
-    // 16 warps owning one ring slot (one CTA per SM)
+    // one token and a long row range per CTA: chunks of 32 rows (few, large bulk copies: each
+    // SM keeps only a handful of them in flight), 4 warps per chunk with 8 rows each, one ring
+    // slot per group of 4 warps (one CTA per SM)
     {
-        const int cw1 = consumer_warps(1);
-        const int ng1 = (N + kCRows1 - 1) / kCRows1;
-        const int grid1 = ng1 < dev.num_sms ? ng1 : dev.num_sms;
-        const uint32_t sb1 = (uint32_t)kCRows1 * ((uint32_t)K / 2 + srow);
-        if (g.tc == 1 && (ng1 + grid1 - 1) / grid1 >= 2 * cw1 &&
-            g.off_ring + (uint32_t)cw1 * sb1 + 2048u <= (uint32_t)dev.smem_optin) {
-            g.wpc = 1;
-            g.crows = kCRows1;
-            g.grid = grid1;
-            g.slot_bytes = sb1;
-            g.slots = cw1;
+        constexpr int kWideWpc = 4;
+        const int cw1 = consumer_warps(1), crows = kCRows1 * kWideWpc, groups = cw1 / kWideWpc;
+        const int ngw = (N + crows - 1) / crows;
+        const int gridw = ngw < dev.num_sms ? ngw : dev.num_sms;
+        const uint32_t sbw = (uint32_t)crows * ((uint32_t)K / 2 + srow);
+        if (g.tc == 1 && (ngw + gridw - 1) / gridw >= 2 * groups &&
+            g.off_ring + (uint32_t)groups * sbw + 2048u <= (uint32_t)dev.smem_optin) {
+            g.wpc = kWideWpc;
+            g.wide = 1;
+            g.crows = crows;
+            g.grid = gridw;
+            g.slot_bytes = sbw;
+            g.slots = groups;
             g.smem = g.off_ring + (uint32_t)g.slots * g.slot_bytes;
             return g;
         }
     }
+    g.wide = 0;
     g.wpc = kWarpsPerChunk;
     g.crows = kCRows;
     const int ngroups = (N + kCRows - 1) / kCRows;
@@ -581,6 +595,7 @@ cudaError_t launch_gemv(const nvfp4_weight& W, const uint16_t* x, int T, uint16_
     P.ngroups = (W.N + g.crows - 1) / g.crows;
     P.wpc = g.wpc;
     P.crows = g.crows;
+    P.wide = g.wide;
     P.slots = g.slots;
     P.slot_bytes = g.slot_bytes;
     P.off_ring = g.off_ring;
