@@ -68,6 +68,7 @@ constexpr int kW = 16;                    // compute warps
 constexpr int kThr = (kW + 1) * 32;       // + the copy warp
 constexpr int kCopyWarp = kW;
 constexpr int kChunks = 4;                // routed-pair copy chunks (one mbarrier each)
+static_assert(kChunks >= 1 && kChunks * 8 <= 32, "the copy warp gives each chunk 8 lanes");
 constexpr int kSlots = NVFP4_MAX_TOPK + 1;
 
 struct T1Params {
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
         {
             const int ch = lane >> 3, piece = (lane >> 2) & 1, part = lane & 3;
             const int qa = q0 + nq * ch / kChunks, qb = q0 + nq * (ch + 1) / kChunks;
-            if (qb > qa) {
+            if (ch < kChunks && qb > qa) {   // lanes of chunks past kChunks issue nothing
                 const int ja = qa / I;
                 const int qs = piece == 0 ? qa : (ja + 1) * I;
                 const int qe = piece == 0 ? min(qb, (ja + 1) * I) : qb;
