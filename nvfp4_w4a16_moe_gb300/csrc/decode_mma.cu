@@ -174,17 +174,44 @@ __device__ __forceinline__ void k_loop(float (&acc)[2][4], const uint8_t* codes0
     }
 }
 
+// Two 16-row tiles, rows [0, 8) + [8, 16) and the same 128 rows further on, over the
+// same K and one n8 block: the K loop runs over the first tile's chunks, then the
+// second's, with the next chunk's loads in flight across the boundary.
+__device__ __forceinline__ void k_loop_tiles(float (&accA)[2][4], float (&accB)[2][4], const uint8_t* codes0,
+                                             const uint8_t* scl0, const uint8_t* codes1, const uint8_t* scl1,
+                                             uint32_t tile_codes, uint32_t tile_scl, int nchunk, const uint8_t* brow0,
+                                             uint32_t q, uint32_t xmask, WChunk c0, WChunk c1, uint64_t pol) {
+    const int n2 = 2 * nchunk;
+    for (int v = 0; v < n2; ++v) {
+        WChunk n0 = c0, n1 = c1;
+        if (v + 1 < n2) {
+            const bool tb = v + 1 >= nchunk;
+            const int jn = tb ? v + 1 - nchunk : v + 1;
+            const uint32_t oc = tb ? tile_codes : 0u, os = tb ? tile_scl : 0u;
+            n0 = load_chunk(codes0 + oc, scl0 + os, jn, pol);
+            n1 = load_chunk(codes1 + oc, scl1 + os, jn, pol);
+        }
+        if (v < nchunk) chunk_mma<1>(accA, c0, c1, brow0, brow0, 64u * v + 16u * q, xmask);
+        else chunk_mma<1>(accB, c0, c1, brow0, brow0, 64u * (v - nchunk) + 16u * q, xmask);
+        c0 = n0;
+        c1 = n1;
+    }
+}
+
 // ------------------------------------------------------------------ router + route
 // logits[t, e] = x[t] . Wg[e] (e < E); gate_logit[t] = x[t] . gs (row E). CTA
-// (bx, by) = 8 rows (a warp each) x the 16 tokens of block by; a lane holds its
-// 16-byte chunks of the row as fp32 and reads the tokens' chunks from shared
-// memory (consecutive lanes, consecutive 16 bytes: conflict-free). Then a ticket
-// per token block: the CTA that finishes last takes the top-k of those tokens, and
-// the token block that finishes last builds the lists. Nothing waits: a CTA that
-// is not last simply exits, and the last one resets its counter for the next call.
+// (bx, by) = rr rows x the 8 tokens of block by (rr = 2, 4 or 8, the fewest rows that
+// keep the grid resident at once): warp w takes row rr bx + w / (8 / rr) and rr of the
+// block's tokens, two per pass (at rr = 2 each warp's chain is one row load and one
+// pass of two dot products). A lane holds its 16-byte chunks of the row
+// as fp32 and reads the tokens' chunks from shared memory (consecutive lanes,
+// consecutive 16 bytes: conflict-free). Then a ticket per token block: the CTA that
+// finishes last takes the top-k of those tokens, and the token block that finishes
+// last builds the lists. Nothing waits: a CTA that is not last simply exits, and the
+// last one resets its counter for the next call.
 __global__ void __launch_bounds__(kThreads)
 router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restrict__ gs,
-                       const uint16_t* __restrict__ x, int T, int E, int H, int k, float* logits,
+                       const uint16_t* __restrict__ x, int T, int E, int H, int k, int rr, float* logits,
                        float* gate_logit, int32_t* ids, float* w, int32_t* ids_out, float* w_out,
                        int32_t* offsets, int32_t* token_list, int32_t* active, int32_t* pass_map,
                        uint32_t* amax, WsHeader* hdr) {
@@ -194,7 +221,9 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = H >> 3;
     const int rows = E + (gs ? 1 : 0);
-    const int r = blockIdx.x * kWarps + warp;
+    const int wpr = kWarps / rr;                          // warps per row
+    const int r = blockIdx.x * rr + warp / wpr;
+    const int tp = rr * (warp % wpr);                     // the warp's first token in the block
     const int t0 = blockIdx.y * kRouterTok;
     const int tc = min(kRouterTok, T - t0);
     const uint16_t* row = r < E ? wg + (size_t)r * H : gs;
@@ -227,9 +256,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
         if (blockIdx.y == 0)
             for (int i = threadIdx.x; i < T * k + T; i += kThreads) amax[T + i] = 0u;
     }
-    if (r < rows) {
-        // one token at a time (a rolled loop keeps the code small: this kernel runs
-        // once per SM, so its instructions are fetched cold)
+    if (r < rows && tp < tc) {
         if (nch <= 256) {
             float wf[8][8];
 #pragma unroll
@@ -243,7 +270,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
                 }
             }
 #pragma unroll 1
-            for (int t = 0; t < tc; t += 2) {   // two tokens per pass: two independent chains
+            for (int t = tp; t < min(tc, tp + rr); t += 2) {   // two tokens per pass: two independent chains
                 const bool two = t + 1 < tc;
                 float a = 0.f, b = 0.f;
 #pragma unroll
@@ -280,7 +307,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
             }
         } else {
 #pragma unroll 1
-            for (int t = 0; t < tc; ++t) {
+            for (int t = tp; t < min(tc, tp + rr); ++t) {
                 float a = 0.f;
 #pragma unroll 1
                 for (int c = lane; c < nch; c += 32) {
@@ -327,7 +354,11 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     __syncthreads();
     if (!s_last) return;
     build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
-    if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
+    if (threadIdx.x == 0) {
+        atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
+        hdr->mt_next[0] = 0u;   // the expert kernels of this call hand out items from 0
+        hdr->mt_next[1] = 0u;
+    }
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -339,14 +370,16 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
 // block: h = silu(ts_g * gate) * (ts_u * up), written in fp32 (entry-major [T*k, I]
 // for the routed experts, [T, Is] for the shared one). hmax keeps each h row's
 // largest magnitude (routed entry e at e, shared token t at T*k + t).
-__global__ void __launch_bounds__(kThreads, 3)
+template <int NBMAX, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ token_list,
                  const int32_t* __restrict__ active, const int32_t* __restrict__ pass_map,
                  const uint32_t* __restrict__ xmax, uint32_t* __restrict__ hmax, float* __restrict__ h,
-                 float* __restrict__ hs) {
+                 float* __restrict__ hs, WsHeader* hdr) {
     extern __shared__ __align__(16) uint8_t stage[];
     __shared__ uint32_t s_hmax[kPass];
+    __shared__ int s_item[2];   // the CTA's next item, by iteration parity
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
     const int H = d.H, k = d.k;
@@ -356,7 +389,8 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
     const int nchunk = H >> 8;
     const uint32_t xmask = 4u * q | (g & 3u);
     const uint64_t pol = l2_evict_first_policy();
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int item = blockIdx.x;   // the first item; then the next one not yet handed out
+    for (int it = 0; item < items; ++it) {
         const uint8_t* codes;
         const uint8_t* scl;
         const int32_t* list;   // routed: the pass's entries; shared: none (tokens first + r)
@@ -402,8 +436,9 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         const uint8_t* sg = scl + (size_t)i * (H / 16) + 4 * q;
         const uint8_t* su = scl + (size_t)(Irows + i) * (H / 16) + 4 * q;
         const WChunk c0 = load_chunk(cg, sg, 0, pol), c1 = load_chunk(cu, su, 0, pol);
-        __syncthreads();   // the previous item is done with the stage and s_hmax
+        __syncthreads();   // the previous item is done with the stage, s_hmax and s_item
         if (threadIdx.x < kPass) s_hmax[threadIdx.x] = 0u;
+        if (NBMAX == 2 && threadIdx.x == 0) s_item[it & 1] = (int)gridDim.x + (int)atomicAdd(&hdr->mt_next[0], 1u);
         {   // x rows of the entries, times 2^k_t, as f16
             const int per_row = H >> 3;
             for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
@@ -419,13 +454,14 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
             }
         }
         __syncthreads();
+        const int next = NBMAX == 2 ? s_item[it & 1] : item + (int)gridDim.x;
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * H * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * H * 2;
-        if (n > 8) k_loop<2>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1, pol);
+        if (NBMAX == 2 && n > 8) k_loop<2>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1, pol);
         else k_loop<1>(acc, cg, sg, cu, su, nchunk, b0, b1, q, xmask, c0, c1, pol);
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
+        for (int nb = 0; nb < NBMAX; ++nb) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int r = 8 * nb + 2 * (int)q + c;
@@ -446,6 +482,7 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         }
         __syncthreads();
         if (threadIdx.x < n) atomicMax(&hmax[hidx(threadIdx.x)], s_hmax[threadIdx.x]);
+        item = next;
     }
 }
 
@@ -456,23 +493,26 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
 // Output rows, fp32, one writer each:
 //   P[entry, n] = w_entry * ts_e * (D_e[n] . h_entry)          (routed)
 //   Ps[t, n]    = sigmoid(gate_t) * ts_s * (Ds[n] . hs_t)       (shared)
-__global__ void __launch_bounds__(kThreads, 3)
+template <int NBMAX, int MINB, int TILES>
+__global__ void __launch_bounds__(kThreads, MINB)
 down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
                const int32_t* __restrict__ token_list, const int32_t* __restrict__ active,
                const int32_t* __restrict__ pass_map, const float* __restrict__ wts,
                const float* __restrict__ gate_logit, const float* __restrict__ h,
                const float* __restrict__ hs, const uint32_t* __restrict__ hmax, float* __restrict__ P,
-               float* __restrict__ Ps) {
+               float* __restrict__ Ps, WsHeader* hdr) {
     extern __shared__ __align__(16) uint8_t stage[];
+    __shared__ int s_item[2];   // the CTA's next item, by iteration parity
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
     const int H = d.H, k = d.k;
-    const int rb_n = H / kDnRows;
+    const int rb_n = H / (TILES * kDnRows);
     const int items_r = pass_map[0] * rb_n;
     const int items = items_r + (d.Is > 0 ? (T + kPass - 1) / kPass * rb_n : 0);
     const uint32_t xmask = 4u * q | (g & 3u);
     const uint64_t pol = l2_evict_first_policy();
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    int item = blockIdx.x;   // the first item; then the next one not yet handed out
+    for (int it = 0; item < items; ++it) {
         const uint8_t* codes;
         const uint8_t* scl;
         const int32_t* list;
@@ -508,13 +548,14 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         }
         auto hrow = [&](int r) { return list ? list[r] : first + r; };
         auto hidx = [&](int r) { return list ? list[r] : T * k + first + r; };
-        const int nr = rb * kDnRows + 16 * warp + (int)g;
+        const int nr = rb * (TILES * kDnRows) + 16 * warp + (int)g;
         const uint8_t* c0p = codes + (size_t)nr * (K / 2) + 32 * q;
         const uint8_t* c1p = codes + (size_t)(nr + 8) * (K / 2) + 32 * q;
         const uint8_t* s0p = scl + (size_t)nr * (K / 16) + 4 * q;
         const uint8_t* s1p = scl + (size_t)(nr + 8) * (K / 16) + 4 * q;
         const WChunk c0 = load_chunk(c0p, s0p, 0, pol), c1 = load_chunk(c1p, s1p, 0, pol);
-        __syncthreads();
+        __syncthreads();   // the previous item is done with the stage and s_item
+        if (NBMAX == 2 && threadIdx.x == 0) s_item[it & 1] = (int)gridDim.x + (int)atomicAdd(&hdr->mt_next[1], 1u);
         {   // h rows of the entries, times 2^k_h, as f16
             const int per_row = K >> 2;
             for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
@@ -526,32 +567,43 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
             }
         }
         __syncthreads();
-        float acc[2][4] = {};
+        const int next = NBMAX == 2 ? s_item[it & 1] : item + (int)gridDim.x;
+        float acc[TILES][2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * K * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * K * 2;
-        if (n > 8) k_loop<2>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
-        else k_loop<1>(acc, c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
+        if constexpr (TILES == 2) {
+            k_loop_tiles(acc[0], acc[1], c0p, s0p, c1p, s1p, (uint32_t)(kDnRows * (K / 2)), (uint32_t)(kDnRows * (K / 16)),
+                         K >> 8, b0, q, xmask, c0, c1, pol);
+        } else {
+            if (NBMAX == 2 && n > 8) k_loop<2>(acc[0], c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
+            else k_loop<1>(acc[0], c0p, s0p, c1p, s1p, K >> 8, b0, b1, q, xmask, c0, c1, pol);
+        }
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
+        for (int tt = 0; tt < TILES; ++tt) {
+            const int nt = nr + tt * kDnRows;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int r = 8 * nb + 2 * (int)q + c;
-                if (r < n) {
-                    const float inv = exp2i(-row_shift(__ldg(hmax + hidx(r))));
-                    if (list) {
-                        const int en = list[r];
-                        const float f = inv * wts[en] * ts;
-                        P[(size_t)en * H + nr] = acc[nb][c] * f;
-                        P[(size_t)en * H + nr + 8] = acc[nb][2 + c] * f;
-                    } else {
-                        const int t = first + r;
-                        const float f = inv * sigmoid_f32(gate_logit[t]) * ts;
-                        Ps[(size_t)t * H + nr] = acc[nb][c] * f;
-                        Ps[(size_t)t * H + nr + 8] = acc[nb][2 + c] * f;
+            for (int nb = 0; nb < NBMAX; ++nb) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int r = 8 * nb + 2 * (int)q + c;
+                    if (r < n) {
+                        const float inv = exp2i(-row_shift(__ldg(hmax + hidx(r))));
+                        if (list) {
+                            const int en = list[r];
+                            const float f = inv * wts[en] * ts;
+                            P[(size_t)en * H + nt] = acc[tt][nb][c] * f;
+                            P[(size_t)en * H + nt + 8] = acc[tt][nb][2 + c] * f;
+                        } else {
+                            const int t = first + r;
+                            const float f = inv * sigmoid_f32(gate_logit[t]) * ts;
+                            Ps[(size_t)t * H + nt] = acc[tt][nb][c] * f;
+                            Ps[(size_t)t * H + nt + 8] = acc[tt][nb][2 + c] * f;
+                        }
                     }
                 }
             }
         }
+        item = next;
     }
 }
 
@@ -613,39 +665,59 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
     uint32_t* hmax = ws.amax + T;
     float* P = ws.part;
     float* Ps = shared ? ws.part + (size_t)T * d.k * d.H : nullptr;
+    // up to 8 tokens: every routed pass has at most 8 entries (a token picks an expert at
+    // most once), so the expert kernels take one n8 block, fit 64 registers and run four CTAs
+    // per SM; the down kernel's items are 256 rows (two tiles per warp). Then every gate/up
+    // and down item of a call is resident at once, with no second wave.
+    const bool small = T <= 8;
     {   // 1. router GEMV (+ the shared gate's pre-activation), top-k, lists, pass map
         const int rows = d.E + (shared ? 1 : 0);
-        const dim3 grid((rows + kWarps - 1) / kWarps, (T + kRouterTok - 1) / kRouterTok);
         const size_t smem = (size_t)(T < kRouterTok ? T : kRouterTok) * d.H * 2;
         err = cudaFuncSetAttribute(router_route_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
+        const int by = (T + kRouterTok - 1) / kRouterTok;
+        const long cap = (long)dev.num_sms * resident_ctas((const void*)router_route_mt_kernel, smem);
+        int rr = 2;   // rows per CTA: the fewest that keep the grid resident at once
+        while (rr < kWarps && (long)((rows + rr - 1) / rr) * by > cap) rr *= 2;
+        const dim3 grid((rows + rr - 1) / rr, by);
         router_route_mt_kernel<<<grid, kThreads, smem, s>>>(
-            d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E, d.H, d.k, ws.logits, ws.gate_logit, ws.ids,
+            d.router_w, shared ? d.sh_gate_w : nullptr, x, T, d.E, d.H, d.k, rr, ws.logits, ws.gate_logit, ws.ids,
             ws.w, ids_out, w_out, ws.offsets, ws.token_list, ws.active, ws.pass_map, ws.amax, ws.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 3. gate/up + SwiGLU
-        const size_t smem = (size_t)kPass * d.H * 2;
-        err = cudaFuncSetAttribute(gateup_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const void* fn = small ? (const void*)gateup_mt_kernel<1, 4> : (const void*)gateup_mt_kernel<2, 3>;
+        const size_t smem = (size_t)(small ? 8 : kPass) * d.H * 2;
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         const long items_ub = (long)passes_routed_ub * (d.I / kGuPairs) +
                               (shared ? (long)passes_shared * (d.Is / kGuPairs) : 0);
-        const long cap = (long)dev.num_sms * resident_ctas((const void*)gateup_mt_kernel, smem);
+        const long cap = (long)dev.num_sms * resident_ctas(fn, smem);
         const int grid = (int)(items_ub < cap ? items_ub : cap);
-        gateup_mt_kernel<<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
-                                                      ws.pass_map, xmax, hmax, h, hs);
+        if (small)
+            gateup_mt_kernel<1, 4><<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
+                                                                ws.pass_map, xmax, hmax, h, hs, ws.hdr);
+        else
+            gateup_mt_kernel<2, 3><<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
+                                                                ws.pass_map, xmax, hmax, h, hs, ws.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 4. down, weighted rows
         const int K = d.I > d.Is ? d.I : d.Is;
-        const size_t smem = (size_t)kPass * K * 2;
-        err = cudaFuncSetAttribute(down_mt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const void* fn = small ? (const void*)down_mt_kernel<1, 4, 2> : (const void*)down_mt_kernel<2, 3, 1>;
+        const size_t smem = (size_t)(small ? 8 : kPass) * K * 2;
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        const long items_ub = (long)(passes_routed_ub + (shared ? passes_shared : 0)) * (d.H / kDnRows);
-        const long cap = (long)dev.num_sms * resident_ctas((const void*)down_mt_kernel, smem);
+        const int rows_item = (small ? 2 : 1) * kDnRows;
+        const long items_ub = (long)(passes_routed_ub + (shared ? passes_shared : 0)) * (d.H / rows_item);
+        const long cap = (long)dev.num_sms * resident_ctas(fn, smem);
         const int grid = (int)(items_ub < cap ? items_ub : cap);
-        down_mt_kernel<<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active, ws.pass_map,
-                                                    ws.w, ws.gate_logit, h, hs, hmax, P, Ps);
+        if (small)
+            down_mt_kernel<1, 4, 2><<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active,
+                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps, ws.hdr);
+        else
+            down_mt_kernel<2, 3, 1><<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active,
+                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps, ws.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 5. combine

@@ -18,86 +18,60 @@ namespace nvfp4 {
 constexpr int kMtPass = 16;          // entries per pass of the multi-token expert kernels
 constexpr int kMtMaxEntries = 512;   // T * k <= 64 * 8
 
-// (v, e) comes before (v2, e2) in routing order.
-__device__ __forceinline__ bool route_before(float v, int e, float v2, int e2) {
-    return v > v2 || (v == v2 && e < e2);
+// Order-preserving 32-bit key of a logit (a larger logit gives a larger key); -0 is
+// taken as +0 first, so equal logits give equal keys.
+__device__ __forceinline__ uint32_t route_key(float f) {
+    const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Order (va, ea), (vb, eb) so the first comes first; selects, no branch.
-__device__ __forceinline__ void route_cas(float& va, int& ea, float& vb, int& eb) {
-    const bool sw = route_before(vb, eb, va, ea);
-    const float v0 = sw ? vb : va, v1 = sw ? va : vb;
-    const int e0 = sw ? eb : ea, e1 = sw ? ea : eb;
-    va = v0; vb = v1; ea = e0; eb = e1;
-}
-
-// Top-k of one token's E logits (lane l holds experts l, l+32, ..., l+224): each
-// lane sorts its eight (bitonic network), then five butterfly rounds each merge a
-// lane's sorted eight with its partner's and keep the first eight: element-wise the
-// better of one list and the other reversed is a bitonic sequence holding the top
-// eight, and three compare-exchange stages sort it. Every lane ends with the same
-// sorted top eight. The chain of dependent steps is short (about 45 compare-
-// exchange or select levels) and branch-free; the butterfly loop stays rolled to
-// keep the code small. Lane j < k writes ids[j] and w[j]. Logits are read through
-// L2 (`ld.cg`) because other blocks wrote them.
+// Top-k of one token's E logits (E <= 256), by one warp. Lane l holds experts 8l .. 8l+7
+// as 64-bit keys (route_key, then 7 - i so that the lower id ranks first among equal
+// logits) and sorts them descending in registers (a 19-exchange merge network). Each of
+// the k rounds takes the largest head over the warp (among equal heads the lowest lane,
+// which holds the lowest ids) and the lane that held it drops it. The result is the
+// routing order: larger logit first, lower expert id first among equal logits. Lane
+// j < k writes ids[j] and w[j]. Logits are read through L2 (`ld.cg`) because other
+// blocks wrote them.
 __device__ __forceinline__ void topk_warp_mt(const float* lg, int E, int k, int32_t* ids, float* w,
                                              int32_t* ids_out, float* w_out) {
     const int lane = threadIdx.x & 31;
-    float v[8];
-    int e[8];
+    unsigned long long kk[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        e[i] = lane + 32 * i;
-        v[i] = e[i] < E ? __ldcg(lg + e[i]) : -INFINITY;
-        if (e[i] >= E) e[i] = 0x7fffffff;
+        const int e = 8 * lane + i;
+        kk[i] = e < E ? ((unsigned long long)route_key(__ldcg(lg + e)) << 3) | (unsigned)(7 - i) : 0ull;
     }
-#pragma unroll
-    for (int size = 2; size <= 8; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    if ((i & size) == 0 || size == 8) route_cas(v[i], e[i], v[j], e[j]);
-                    else route_cas(v[j], e[j], v[i], e[i]);
-                }
-            }
-        }
-    }
+#define MT_CX(a, b) { const unsigned long long hi_ = max(kk[a], kk[b]), lo_ = min(kk[a], kk[b]); kk[a] = hi_; kk[b] = lo_; }
+    MT_CX(0, 1) MT_CX(2, 3) MT_CX(4, 5) MT_CX(6, 7)
+    MT_CX(0, 2) MT_CX(1, 3) MT_CX(4, 6) MT_CX(5, 7)
+    MT_CX(1, 2) MT_CX(5, 6)
+    MT_CX(0, 4) MT_CX(1, 5) MT_CX(2, 6) MT_CX(3, 7)
+    MT_CX(2, 4) MT_CX(3, 5)
+    MT_CX(1, 2) MT_CX(3, 4) MT_CX(5, 6)
+#undef MT_CX
+    int my_e = 0;
+    float my_v = 0.f, vmax = 0.f;
 #pragma unroll 1
-    for (int o = 1; o < 32; o <<= 1) {
-        float pv[8];
-        int pe[8];
+    for (int j = 0; j < k; ++j) {
+        const uint32_t hk = (uint32_t)(kk[0] >> 3);
+        const uint32_t wb = __reduce_max_sync(0xffffffffu, hk);
+        const int win = __ffs(__ballot_sync(0xffffffffu, hk == wb)) - 1;
+        const int e = __shfl_sync(0xffffffffu, 8 * lane + 7 - (int)((uint32_t)kk[0] & 7u), win);
+        if (lane == win) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            pv[i] = __shfl_xor_sync(0xffffffffu, v[i], o);
-            pe[i] = __shfl_xor_sync(0xffffffffu, e[i], o);
+            for (int i = 0; i < 7; ++i) kk[i] = kk[i + 1];
+            kk[7] = 0ull;
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const bool mine = route_before(v[i], e[i], pv[7 - i], pe[7 - i]);
-            v[i] = mine ? v[i] : pv[7 - i];
-            e[i] = mine ? e[i] : pe[7 - i];
-        }
-#pragma unroll
-        for (int stride = 4; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = i ^ stride;
-                if (j > i) route_cas(v[i], e[i], v[j], e[j]);
-            }
-        }
+        const float v = route_key_value(wb);
+        if (j == 0) vmax = v;
+        if (lane == j) { my_e = e; my_v = v; }
     }
-    // w_j = exp(l_j - l_max) / sum_{j' < k} exp(l_j' - l_max), summed in rank order;
-    // lane j takes element j of the (identical) lists
-    float my_v = v[0];
-    int my_e = e[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j) {
-        if (lane == j) { my_v = v[j]; my_e = e[j]; }
-    }
-    const float ex = lane < k ? expf(my_v - v[0]) : 0.f;
+    // w_j = exp(l_j - l_max) / sum_{j' < k} exp(l_j' - l_max), summed in rank order
+    const float ex = lane < k ? expf(my_v - vmax) : 0.f;
     float sum = 0.f;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
@@ -129,7 +103,7 @@ __device__ __forceinline__ void build_lists_block(ListsSmem& S, const int32_t* i
                                                   int32_t* pass_map) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = (total + 31) >> 5;
-    for (int i = tid; i < NVFP4_MAX_EXPERTS * (kMtMaxEntries / 32); i += 256) (&S.mask[0][0])[i] = 0u;
+    for (int i = tid; i < NVFP4_MAX_EXPERTS * nw; i += 256) S.mask[i / nw][i - (i / nw) * nw] = 0u;
     __syncthreads();
     for (int i = tid; i < total; i += 256) {
         const int e = __ldcg(ids + i);

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workload as wl
 from harness import check_layer_parity, gpu_layer
 
@@ -33,6 +34,29 @@ def test_small_layer_every_token(nv, T):
     x = wl.activations(200 + T, T, SM.H)
     y, ids, w = _forward(nv, layer, x)
     check_layer_parity(L, x, y, ids, w)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_exact_ties_rank_lower_expert_first(nv, T):
+    """Router rows repeated in threes (experts 3j, 3j+1, 3j+2 share a row): every token's
+    logits tie in threes and its 8th and 9th largest are two members of one triple, so the
+    top-8 must keep the lower id of the two. Ids, in rank order, equal the oracle's
+    (larger logit first, lower expert id first among equal logits: lynn-engine README,
+    P35 note); the renormalised weights agree within 1e-5. T = 1 runs the single-token
+    kernel, 8 and 64 the multi-token router."""
+    shape = wl.MoEShape(H=256, E=256, k=8, I=256, Is=256)
+    L = wl.LayerInputs(shape, seed=400 + T)
+    layer = gpu_layer(L)
+    tied = L.router_w("cpu")[torch.arange(shape.E) // 3 * 3].contiguous()
+    layer.router_w.copy_(tied.cuda())
+    x = wl.activations(400 + T, T, shape.H)
+    y, ids, w = _forward(nv, layer, x)
+    ids_o, w_o, _ = oracle.route(oracle.router_logits(x, tied), shape.k)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert float(np.abs(w.cpu().numpy() - w_o).max()) <= 1e-5
+    # the boundary really falls inside a triple: two of its three members selected
+    split = [sum(1 for e in row if e // 3 == row[-1] // 3) for row in ids_o.tolist()]
+    assert 2 in split
 
 
 def test_small_layer_skewed_routing_multi_pass(nv):
