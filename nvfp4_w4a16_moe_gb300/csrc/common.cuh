@@ -17,8 +17,7 @@ namespace nvfp4 {
 // launches (one 64-bit counter never wraps in practice); `route_tickets` count
 // the router blocks of one multi-token call that are done (one counter per token
 // block, then one over token blocks) and are reset to 0 by the block that
-// finishes last; `mt_next` count the items of the multi-token gate/up and down
-// kernels taken beyond their first (one per CTA), reset by that same block.
+// finishes last.
 constexpr int kRouteTicketBlocks = 8;
 struct alignas(256) WsHeader {
     uint32_t status;
@@ -26,8 +25,7 @@ struct alignas(256) WsHeader {
     unsigned long long barrier;
     unsigned int amax_bits;      // nvfp4_pack: max |w| as fp32 bits
     unsigned int route_tickets[kRouteTicketBlocks + 1];
-    unsigned int mt_next[2];     // multi-token gate/up and down: items handed out so far
-    unsigned int pad1[48];
+    unsigned int pad1[50];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -354,11 +354,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     __syncthreads();
     if (!s_last) return;
     build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
-    if (threadIdx.x == 0) {
-        atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
-        hdr->mt_next[0] = 0u;   // the expert kernels of this call hand out items from 0
-        hdr->mt_next[1] = 0u;
-    }
+    if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -376,10 +372,9 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ token_list,
                  const int32_t* __restrict__ active, const int32_t* __restrict__ pass_map,
                  const uint32_t* __restrict__ xmax, uint32_t* __restrict__ hmax, float* __restrict__ h,
-                 float* __restrict__ hs, WsHeader* hdr) {
+                 float* __restrict__ hs) {
     extern __shared__ __align__(16) uint8_t stage[];
     __shared__ uint32_t s_hmax[kPass];
-    __shared__ int s_item[2];   // the CTA's next item, by iteration parity
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
     const int H = d.H, k = d.k;
@@ -389,8 +384,7 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
     const int nchunk = H >> 8;
     const uint32_t xmask = 4u * q | (g & 3u);
     const uint64_t pol = l2_evict_first_policy();
-    int item = blockIdx.x;   // the first item; then the next one not yet handed out
-    for (int it = 0; item < items; ++it) {
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const uint8_t* codes;
         const uint8_t* scl;
         const int32_t* list;   // routed: the pass's entries; shared: none (tokens first + r)
@@ -436,9 +430,8 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         const uint8_t* sg = scl + (size_t)i * (H / 16) + 4 * q;
         const uint8_t* su = scl + (size_t)(Irows + i) * (H / 16) + 4 * q;
         const WChunk c0 = load_chunk(cg, sg, 0, pol), c1 = load_chunk(cu, su, 0, pol);
-        __syncthreads();   // the previous item is done with the stage, s_hmax and s_item
+        __syncthreads();   // the previous item is done with the stage and s_hmax
         if (threadIdx.x < kPass) s_hmax[threadIdx.x] = 0u;
-        if (NBMAX == 2 && threadIdx.x == 0) s_item[it & 1] = (int)gridDim.x + (int)atomicAdd(&hdr->mt_next[0], 1u);
         {   // x rows of the entries, times 2^k_t, as f16
             const int per_row = H >> 3;
             for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
@@ -454,7 +447,6 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
             }
         }
         __syncthreads();
-        const int next = NBMAX == 2 ? s_item[it & 1] : item + (int)gridDim.x;
         float acc[2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * H * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * H * 2;
@@ -482,7 +474,6 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
         }
         __syncthreads();
         if (threadIdx.x < n) atomicMax(&hmax[hidx(threadIdx.x)], s_hmax[threadIdx.x]);
-        item = next;
     }
 }
 
@@ -500,9 +491,8 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
                const int32_t* __restrict__ pass_map, const float* __restrict__ wts,
                const float* __restrict__ gate_logit, const float* __restrict__ h,
                const float* __restrict__ hs, const uint32_t* __restrict__ hmax, float* __restrict__ P,
-               float* __restrict__ Ps, WsHeader* hdr) {
+               float* __restrict__ Ps) {
     extern __shared__ __align__(16) uint8_t stage[];
-    __shared__ int s_item[2];   // the CTA's next item, by iteration parity
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t g = lane >> 2, q = lane & 3;
     const int H = d.H, k = d.k;
@@ -511,8 +501,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
     const int items = items_r + (d.Is > 0 ? (T + kPass - 1) / kPass * rb_n : 0);
     const uint32_t xmask = 4u * q | (g & 3u);
     const uint64_t pol = l2_evict_first_policy();
-    int item = blockIdx.x;   // the first item; then the next one not yet handed out
-    for (int it = 0; item < items; ++it) {
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const uint8_t* codes;
         const uint8_t* scl;
         const int32_t* list;
@@ -554,8 +543,7 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
         const uint8_t* s0p = scl + (size_t)nr * (K / 16) + 4 * q;
         const uint8_t* s1p = scl + (size_t)(nr + 8) * (K / 16) + 4 * q;
         const WChunk c0 = load_chunk(c0p, s0p, 0, pol), c1 = load_chunk(c1p, s1p, 0, pol);
-        __syncthreads();   // the previous item is done with the stage and s_item
-        if (NBMAX == 2 && threadIdx.x == 0) s_item[it & 1] = (int)gridDim.x + (int)atomicAdd(&hdr->mt_next[1], 1u);
+        __syncthreads();
         {   // h rows of the entries, times 2^k_h, as f16
             const int per_row = K >> 2;
             for (int idx = threadIdx.x; idx < n * per_row; idx += kThreads) {
@@ -567,7 +555,6 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
             }
         }
         __syncthreads();
-        const int next = NBMAX == 2 ? s_item[it & 1] : item + (int)gridDim.x;
         float acc[TILES][2][4] = {};
         const uint8_t* b0 = stage + (size_t)g * K * 2;
         const uint8_t* b1 = stage + (size_t)(g + 8) * K * 2;
@@ -603,7 +590,6 @@ down_mt_kernel(moe_layer_desc d, int T, const int32_t* __restrict__ offsets,
                 }
             }
         }
-        item = next;
     }
 }
 
@@ -696,10 +682,10 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
         const int grid = (int)(items_ub < cap ? items_ub : cap);
         if (small)
             gateup_mt_kernel<1, 4><<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
-                                                                ws.pass_map, xmax, hmax, h, hs, ws.hdr);
+                                                                ws.pass_map, xmax, hmax, h, hs);
         else
             gateup_mt_kernel<2, 3><<<grid, kThreads, smem, s>>>(d, x, T, ws.offsets, ws.token_list, ws.active,
-                                                                ws.pass_map, xmax, hmax, h, hs, ws.hdr);
+                                                                ws.pass_map, xmax, hmax, h, hs);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 4. down, weighted rows
@@ -714,10 +700,10 @@ cudaError_t launch_moe_decode_mma(const moe_layer_desc& d, const uint16_t* x, in
         const int grid = (int)(items_ub < cap ? items_ub : cap);
         if (small)
             down_mt_kernel<1, 4, 2><<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active,
-                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps, ws.hdr);
+                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps);
         else
             down_mt_kernel<2, 3, 1><<<grid, kThreads, smem, s>>>(d, T, ws.offsets, ws.token_list, ws.active,
-                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps, ws.hdr);
+                                                                 ws.pass_map, ws.w, ws.gate_logit, h, hs, hmax, P, Ps);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     {   // 5. combine
