@@ -292,12 +292,23 @@ NVFP4_API size_t moe_layer_residual_workspace_size(const moe_layer_desc* d, int3
  *   All calls on a device share the one array: calls that can overlap on the
  *   GPU (different streams without ordering) race and must not be made.
  *   A layer whose scratch (moe_layer_workspace_size) exceeds 8 MiB is rejected
- *   with NVFP4_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. Device-side
- *   wait timeouts are recorded in the array but cannot be read back.
+ *   with NVFP4_ERR_WORKSPACE_TOO_SMALL before anything is enqueued. A device-side
+ *   wait that ran out is recorded in the array's status word: read it with
+ *   nvfp4_noalloc_status before the next call, which clears the array.
  */
 NVFP4_API nvfp4_status moe_layer_forward_noalloc(const moe_layer_desc* d, const uint16_t* x, int32_t T,
                                                  uint16_t* y, int32_t* topk_ids_out, float* topk_w_out,
                                                  void* stream);
+
+/*
+ * nvfp4_noalloc_status - the device status word of the static scratch array of
+ * moe_layer_forward_noalloc on the current device: synchronises `stream`, then returns
+ * NVFP4_OK or the status a kernel of the last noalloc call recorded there
+ * (NVFP4_ERR_DEVICE_TIMEOUT when a bounded wait ran out; the call's outputs are then not
+ * valid). clear != 0 resets the word to NVFP4_OK. NVFP4_ERR_CUDA when the array's
+ * address or the copy fails.
+ */
+NVFP4_API nvfp4_status nvfp4_noalloc_status(int32_t clear, void* stream);
 
 /*
  * nvfp4_scale_kind_of - which block-scale contract a stored NVFP4 matrix uses, from its

@@ -138,6 +138,8 @@ lib.nvfp4_version.restype = _i32
 lib.nvfp4_version.argtypes = []
 lib.moe_layer_forward_noalloc.restype = _i32
 lib.moe_layer_forward_noalloc.argtypes = [ctypes.POINTER(MoELayerDescC), _P, _i32, _P, _P, _P, _P]
+lib.nvfp4_noalloc_status.restype = _i32
+lib.nvfp4_noalloc_status.argtypes = [_i32, _P]
 
 
 def _check(status: int, where: str):
@@ -430,6 +432,13 @@ def moe_layer_forward_noalloc(layer: MoELayer, x: torch.Tensor, y: Optional[torc
     if want_route:
         return y, ids_out, w_out
     return y
+
+
+def noalloc_status(clear: bool = True, stream=None) -> int:
+    """The status word a kernel of the last moe_layer_forward_noalloc call on the current
+    device recorded (NVFP4_OK, or NVFP4_ERR_DEVICE_TIMEOUT when a bounded wait ran out);
+    synchronises the stream first."""
+    return lib.nvfp4_noalloc_status(1 if clear else 0, _stream(stream))
 
 
 def set_device_wait_limit(spins: int):

@@ -67,4 +67,11 @@ nvfp4_status moe_layer_forward_noalloc(const moe_layer_desc* d, const uint16_t* 
     return moe_layer_forward(d, x, T, y, topk_ids_out, topk_w_out, scratch, kNoallocScratchBytes, stream);
 }
 
+nvfp4_status nvfp4_noalloc_status(int32_t clear, void* stream) {
+    void* scratch = nullptr;
+    const nvfp4_status st = scratch_address(&scratch);
+    if (st != NVFP4_OK) return st;
+    return nvfp4_get_device_status(scratch, clear, stream);   // the array starts with the workspace header
+}
+
 }  // extern "C"

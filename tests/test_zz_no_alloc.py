@@ -62,6 +62,31 @@ def test_noalloc_large_then_small_then_large(nv):
         assert torch.equal(ids, ids_ref) and torch.equal(w, w_ref), T
 
 
+def test_noalloc_status_reports_a_timeout(nv):
+    """The static scratch's status word is readable: OK after a normal call; with the wait
+    limit at 1 ns the single-token grid form's exchange polls run out (it always polls
+    before its peers publish), the timeout is recorded and read back, clearing works, and
+    the next call (which clears the scratch) is exact again."""
+    from harness import single_token_form
+    L = wl.LayerInputs(wl.SMALL256, seed=13)
+    layer = gpu_layer(L)
+    x = wl.activations(13, 1, wl.SMALL256.H).cuda()
+    y_ref = nv.moe_layer_forward(layer, x)
+    with single_token_form(nv, 1):
+        _noalloc(nv, layer, x)
+        assert nv.noalloc_status() == nv.NVFP4_OK
+        try:
+            nv.set_device_wait_limit(1)
+            _noalloc(nv, layer, x)
+            assert nv.noalloc_status(clear=True) == nv.NVFP4_ERR_DEVICE_TIMEOUT
+            assert nv.noalloc_status() == nv.NVFP4_OK
+        finally:
+            nv.set_device_wait_limit(0)
+        y, _, _ = _noalloc(nv, layer, x)
+        assert nv.noalloc_status() == nv.NVFP4_OK
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
 def test_noalloc_rejects_oversized_scratch(nv):
     L = wl.LayerInputs(wl.QWEN36_35B_A3B, seed=0)
     layer = gpu_layer(L)
