@@ -358,7 +358,8 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
 }
 
 // ------------------------------------------------------------------ gate/up
-// Item = (slot pass, block of 64 row pairs). Routed passes come from the pass map
+// Item = (slot pass, block of 64 row pairs); NBMAX n8 entry blocks at most (1 when a
+// call has at most 8 tokens, so every pass has at most 8 entries). Routed passes come from the pass map
 // (active slot a, entries [16 pi, 16 pi + 16) of expert a's list); the shared
 // expert's pass pi is tokens [16 pi, 16 pi + 16). Warp w takes gate rows
 // i0 + 8w + g as fragment rows 0-7 and the matching up rows as rows 8-15, so lane
@@ -478,9 +479,10 @@ gateup_mt_kernel(moe_layer_desc d, const uint16_t* __restrict__ x, int T,
 }
 
 // ------------------------------------------------------------------ down
-// Item = (slot pass, block of 128 output rows). Warp w takes rows
-// nr = 128 rb + 16w + g (fragment rows 0-7) and nr + 8 (rows 8-15) over K = I
-// (Is for the shared expert); the entries' h rows are staged as f16 times 2^k_h.
+// Item = (slot pass, block of 128 TILES output rows). Warp w takes rows
+// nr = 128 TILES rb + 16w + g (fragment rows 0-7) and nr + 8 (rows 8-15) over K = I
+// (Is for the shared expert), and with TILES = 2 the same rows 128 further on in the
+// same K loop; the entries' h rows are staged as f16 times 2^k_h.
 // Output rows, fp32, one writer each:
 //   P[entry, n] = w_entry * ts_e * (D_e[n] . h_entry)          (routed)
 //   Ps[t, n]    = sigmoid(gate_t) * ts_s * (Ds[n] . hs_t)       (shared)
