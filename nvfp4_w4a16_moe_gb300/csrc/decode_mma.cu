@@ -339,12 +339,20 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     }
     __syncthreads();
     if (!s_last) return;
+    // one token block (T <= 8): this CTA is also the last overall, keeps the ids in shared
+    // memory for the lists and skips the second ticket
+    const bool one_block = gridDim.y == 1;
     for (int t = t0 + warp; t < t0 + tc; t += kWarps) {
         const size_t o = (size_t)t * k;
         topk_warp_mt(logits + (size_t)t * E, E, k, ids + o, w + o, ids_out ? ids_out + o : nullptr,
-                          w_out ? w_out + o : nullptr);
+                     w_out ? w_out + o : nullptr, one_block ? S.ids + o : nullptr);
     }
     __syncthreads();
+    if (one_block) {
+        if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[0], 0u);
+        build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map, true);
+        return;
+    }
     if (threadIdx.x == 0) {
         __threadfence();
         atomicExch(&hdr->route_tickets[blockIdx.y], 0u);
@@ -353,7 +361,7 @@ router_route_mt_kernel(const uint16_t* __restrict__ wg, const uint16_t* __restri
     }
     __syncthreads();
     if (!s_last) return;
-    build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map);
+    build_lists_block(S, ids, T * k, E, offsets, token_list, active, pass_map, false);
     if (threadIdx.x == 0) atomicExch(&hdr->route_tickets[kRouteTicketBlocks], 0u);
 }
 

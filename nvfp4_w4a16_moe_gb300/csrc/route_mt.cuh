@@ -34,10 +34,10 @@ __device__ __forceinline__ float route_key_value(uint32_t key) {
 // the k rounds takes the largest head over the warp (among equal heads the lowest lane,
 // which holds the lowest ids) and the lane that held it drops it. The result is the
 // routing order: larger logit first, lower expert id first among equal logits. Lane
-// j < k writes ids[j] and w[j]. Logits are read through L2 (`ld.cg`) because other
-// blocks wrote them.
+// j < k writes ids[j] and w[j] (and sids[j] when sids is not null). Logits are read
+// through L2 (`ld.cg`) because other blocks wrote them.
 __device__ __forceinline__ void topk_warp_mt(const float* lg, int E, int k, int32_t* ids, float* w,
-                                             int32_t* ids_out, float* w_out) {
+                                             int32_t* ids_out, float* w_out, int* sids) {
     const int lane = threadIdx.x & 31;
     unsigned long long kk[8];
 #pragma unroll
@@ -79,6 +79,7 @@ __device__ __forceinline__ void topk_warp_mt(const float* lg, int E, int k, int3
         const float wj = ex / sum;
         ids[lane] = my_e;
         w[lane] = wj;
+        if (sids) sids[lane] = my_e;
         if (ids_out) ids_out[lane] = my_e;
         if (w_out) w_out[lane] = wj;
     }
@@ -92,22 +93,28 @@ struct ListsSmem {
     int wsum[3][NVFP4_MAX_EXPERTS / 32];
 };
 
-// Per-expert lists of the total = T*k entries (ids read through L2), by one block
-// of exactly 256 threads. Entry i of expert e goes to offsets[e] + (number of
+// Per-expert lists of the total = T*k entries, by one block of exactly 256 threads;
+// the ids are read through L2, or are already in S.ids (ids_in_smem: written by this
+// block before a barrier). Entry i of expert e goes to offsets[e] + (number of
 // entries i' < i of expert e): a stable counting sort. active[0] = A, active[1+a]
 // = the a-th expert with entries (ascending); pass_map[0] = P, pass_map[1+p] =
 // (active slot << 8) | pass, a pass being up to kMtPass consecutive entries of
 // one expert's list.
 __device__ __forceinline__ void build_lists_block(ListsSmem& S, const int32_t* ids, int total, int E,
                                                   int32_t* offsets, int32_t* token_list, int32_t* active,
-                                                  int32_t* pass_map) {
+                                                  int32_t* pass_map, bool ids_in_smem) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = (total + 31) >> 5;
     for (int i = tid; i < NVFP4_MAX_EXPERTS * nw; i += 256) S.mask[i / nw][i - (i / nw) * nw] = 0u;
     __syncthreads();
     for (int i = tid; i < total; i += 256) {
-        const int e = __ldcg(ids + i);
-        S.ids[i] = e;
+        int e;
+        if (ids_in_smem) {
+            e = S.ids[i];
+        } else {
+            e = __ldcg(ids + i);
+            S.ids[i] = e;
+        }
         atomicOr(&S.mask[e][i >> 5], 1u << (i & 31));
     }
     __syncthreads();
