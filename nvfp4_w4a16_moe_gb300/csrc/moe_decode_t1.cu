@@ -30,7 +30,7 @@
 //   router rows                 bf16 dot products -> logit words (tag, value)
 //   shared pairs                hs words, computed while the other CTAs' logits arrive
 //   top-k                       every CTA gathers the E logits and takes the top-k itself
-//   routed copies               the CTA's routed pairs (4 chunks, one mbarrier each) and
+//   routed copies               the CTA's routed pairs (2 chunks, one mbarrier each) and
 //                               its down rows of the k routed experts
 //   routed pairs                one warp per (gate, up) pair as its chunk lands -> h words
 //   h                           every CTA gathers the k*I + Is words, scales each slot by
@@ -67,7 +67,9 @@ namespace {
 constexpr int kW = 16;                    // compute warps
 constexpr int kThr = (kW + 1) * 32;       // + the copy warp
 constexpr int kCopyWarp = kW;
-constexpr int kChunks = 4;                // routed-pair copy chunks (one mbarrier each)
+constexpr int kChunks = 2;                // routed-pair copy chunks (one mbarrier each; 2 measured
+                                          // faster than 1 or 4: fewer, larger bulk copies, and the
+                                          // first half of the pairs starts while the second lands)
 static_assert(kChunks >= 1 && kChunks * 8 <= 32, "the copy warp gives each chunk 8 lanes");
 constexpr int kSlots = NVFP4_MAX_TOPK + 1;
 
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(kThr, 1) moe_decode_t1_kernel(T1Params P) {
     const uint8_t* gu_s = static_cast<const uint8_t*>(d.gu_scales);
     const uint32_t rowI = I / 2, srowI = I / 16 * sb;
     if (warp == kCopyWarp) {
-        // chunk ch holds local pairs [nq ch / 4, nq (ch+1) / 4): at most two slots ("pieces");
+        // chunk ch holds local pairs [nq ch / kChunks, nq (ch+1) / kChunks): at most two slots ("pieces");
         // lane = 8 ch + 4 piece + part issues one contiguous copy (gate codes, up codes,
         // gate scales, up scales) of the piece's pairs
         if (lane < kChunks) {
