@@ -105,12 +105,18 @@ def test_qwen_64_tokens_deterministic(nv):
 def test_small_layer_activation_scale(nv, scale):
     """Activations far from unit scale (exact power-of-two multiples of the usual
     draw): at 2^16 a plain f16 conversion of the token rows would overflow, so this
-    checks the per-row power-of-two staging of x and h on the tensor-core path. The
-    router's fp32 logit error grows with the activations, so the logit gap below
-    which a token counts as a near tie grows with them too."""
+    checks the per-row power-of-two staging of x and h on the tensor-core path.
+    A power-of-two scale of x scales every fp32 logit exactly (no overflow or
+    subnormal at these scales), so the routing equals the unscaled call's id for id,
+    and the near-tie gap scales with the logits: 1e-3 times the scale. No token of
+    this draw is that close, so every token's ids are checked against the oracle."""
     L = wl.LayerInputs(SM, seed=29)
     layer = gpu_layer(L)
-    x = (wl.activations(29, 12, SM.H).float() * scale).to(torch.bfloat16)
+    x1 = wl.activations(29, 12, SM.H)
+    x = (x1.float() * scale).to(torch.bfloat16)
     y, ids, w = _forward(nv, layer, x)
+    _, ids1, _ = _forward(nv, layer, x1)
     assert torch.isfinite(y.float()).all()
-    check_layer_parity(L, x, y, ids, w, gap_min=1e-3 * max(1.0, scale))
+    assert torch.equal(ids, ids1)
+    _, _, n_near = check_layer_parity(L, x, y, ids, w, gap_min=1e-3 * scale)
+    assert n_near == 0
