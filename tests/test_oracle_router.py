@@ -78,3 +78,21 @@ def test_route_rejects_bad_k(orc):
         orc.route(np.zeros((1, 4)), 5)
     with pytest.raises(ValueError):
         orc.route(np.zeros((1, 4)), 0)
+
+
+def test_logit_gap_is_kth_minus_next(orc):
+    """logit_gap (which tokens count as near ties in the parity tests): the k-th largest logit
+    minus the (k+1)-th, whatever the order of the experts; infinite when every expert is
+    selected."""
+    lg = np.array([[0.5, 3.0, -1.0, 2.0, 2.75],      # sorted: 3, 2.75, 2, 0.5, -1
+                   [1.0, 1.0, 1.0, 0.0, -2.0]])     # an exact tie at the boundary
+    assert np.allclose(orc.logit_gap(lg, 1), [0.25, 0.0])
+    assert np.allclose(orc.logit_gap(lg, 2), [0.75, 0.0])
+    assert np.allclose(orc.logit_gap(lg, 3), [1.5, 1.0])
+    assert np.all(np.isinf(orc.logit_gap(lg, 5)))
+    rng = np.random.default_rng(3)
+    r = rng.standard_normal((50, 16))
+    for k in (1, 4, 8):
+        s = -np.sort(-r, axis=1)
+        assert np.array_equal(orc.logit_gap(r, k), s[:, k - 1] - s[:, k])
+        assert np.array_equal(orc.logit_gap(r[:, rng.permutation(16)], k), orc.logit_gap(r, k))
